@@ -1,0 +1,392 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole path over synthetic inputs resident in HBM:
+  * fused prefill, B=4 H=16 Nq=Nk=2048 d=64 scale=1/8, non-causal, then causal
+    (the headline TFLOP/s workload), and
+  * split-KV decode, B=64 H=32 Nk=8192 d=128, 16 splits (split + merge kernels).
+value  = prefill TFLOP/s (4*B*H*Nq*Nk*d per non-causal launch, half for causal,
+         summed over both launches, divided by their device time);
+decode = HBM GB/s of the decode kernels (K + V + q + o + lse bytes / time).
+Every timed launch is bracketed by CUDA events on the launching stream; the
+L2 (129 MB) is flushed between steps by writing a 256 MB buffer outside the
+events (the prefill inputs, 67 MB, would otherwise stay L2-resident).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs the same per-GPU workload (weak scaling, no
+data-path collective); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (prefill) & HBM GB/s (decode) on 1 GB300, % of roofline"
+PREFILL = "prefill_2k"
+DECODE = "decode_8k"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_hash(name: str) -> str:
+    src = os.path.join(ROOT, "io_aware_exact_fa_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for f in (src, os.path.join(ROOT, "io_aware_exact_fa_gb300", "csrc", "fa_ptx.cuh"),
+              os.path.join(ROOT, "io_aware_exact_fa_gb300", "csrc", "fa_common.cuh")):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    rec = json.load(open(PROFILE_TRAFFIC)).get(workload)
+    if not rec or rec.get("source_hash") != kernel_hash(kernel_file):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.t = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = self.samples
+        if self.window:
+            inside = [r for r in rows if self.window[0] - 0.06 <= r[0] <= self.window[1] + 0.06]
+            rows = inside or rows
+        if not rows:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, f in rows:
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, val in zip(names[1:], f[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_prefill_sample(w, budget_s: float):
+    """Time the fp64 oracle on whole heads of the prefill workload (non-causal
+    and causal alternately) until ``budget_s`` is spent; returns (flops, seconds, heads)."""
+    import numpy as np
+    import torch
+    from io_aware_exact_fa_gb300 import workloads as W
+    from oracle import attention as A
+    q, k, v = W.make_qkv(1, 2, w.Nq, w.Nk, w.d, seed=0)
+    qs = [q[0, h].to(torch.float64).numpy() for h in range(2)]
+    ks = [k[0, h].to(torch.float64).numpy() for h in range(2)]
+    vs = [v[0, h].to(torch.float64).numpy() for h in range(2)]
+    per_head = 4.0 * w.Nq * w.Nk * w.d
+    flops, heads, t0 = 0.0, 0, time.perf_counter()
+    while True:
+        causal = heads % 2 == 1
+        A.attend_head(qs[heads % 2], ks[heads % 2], vs[heads % 2], w.scale, causal)
+        flops += per_head / 2 if causal else per_head
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or heads >= 64:
+            return flops, el, heads
+
+
+# --------------------------------------------------------------- reference
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from io_aware_exact_fa_gb300 import workloads as W
+    w = W.WORKLOADS[PREFILL]
+    for _ in range(args.warmup):
+        oracle_prefill_sample(w, 0.0)
+    flops = secs = 0.0
+    heads = 0
+    budget = max(1.0, 60.0 / max(1, args.steps))
+    for _ in range(args.steps):
+        f, s, h = oracle_prefill_sample(w, budget)
+        flops += f
+        secs += s
+        heads += h
+    value = flops / secs / 1e12
+    sample = f"{heads} whole heads of {w.name} (Nq=Nk={w.Nk}, d={w.d}), non-causal/causal alternating, fp64 NumPy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": [False, True], "oracle": "oracle/attention.py attend_head"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from io_aware_exact_fa_gb300 import build as B
+    B.build()
+    from io_aware_exact_fa_gb300 import fa, workloads as W
+
+    wp = W.WORKLOADS[PREFILL]
+    wd = W.WORKLOADS[DECODE]
+    q, k, v = W.make_qkv(wp.B, wp.H, wp.Nq, wp.Nk, wp.d, seed=rank, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(wp.B, wp.H, wp.Nq, dtype=torch.float32, device=dev)
+    dq, dk, dv = W.make_qkv(wd.B, wd.H, 1, wd.Nk, wd.d, seed=1000 + rank, device="cuda")
+    do = torch.empty_like(dq)
+    dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.decode_workspace_size(wd.B, wd.H, wd.d, wd.num_splits), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def prefill(causal):
+        fa.fwd(q, k, v, scale=wp.scale, causal=causal, out=o, lse=lse)
+
+    def decode():
+        fa.decode(dq, dk, dv, scale=wd.scale, num_splits=wd.num_splits, workspace=ws, out=do, lse=dlse)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        prefill(False)
+        prefill(True)
+        decode()
+    torch.cuda.synchronize()
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    launches0 = fa.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()                     # outside the events: evicts the prefill inputs from L2
+        e = ev[i]
+        e[0].record(stream)
+        prefill(False)
+        e[1].record(stream)
+        prefill(True)
+        e[2].record(stream)
+        decode()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall1 = time.time()
+    launches = fa.launch_count() - launches0
+    sampler.mark(t_wall0, t_wall1)
+    clocks = sampler.stop()
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    t_nc = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t_c = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    t_d = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    times = torch.tensor([t_nc, t_c, t_d], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    t_nc, t_c, t_d = times.tolist()
+    K = args.steps
+    f_nc, f_c = wp.flops(False), wp.flops(True)
+    prefill_tflops = world * K * (f_nc + f_c) / (t_nc + t_c) / 1e12
+    kernel_tflops = K * (f_nc + f_c) / (t_nc + t_c) / 1e12          # per launch average, this GPU
+    dec_bytes = wd.io_bytes()
+    decode_gbs = world * K * dec_bytes / t_d / 1e9
+    peaks = measured_peaks()
+
+    # ---- end to end through the public API with pinned host buffers
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    ho2 = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl2 = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hdq = dq.cpu().pin_memory()
+    hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
+    hdl = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
+    e2e_steps = max(3, min(K, 20))
+    torch.cuda.synchronize()
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.zero_()
+        ee[i][0].record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        prefill(False)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        prefill(True)
+        ho2.copy_(o, non_blocking=True)
+        hl2.copy_(lse, non_blocking=True)
+        ee[i][1].record(stream)
+        dq.copy_(hdq, non_blocking=True)
+        decode()
+        hdo.copy_(do, non_blocking=True)
+        hdl.copy_(dlse, non_blocking=True)
+        ee[i][2].record(stream)
+    torch.cuda.synchronize()
+    te_p = sum(e[0].elapsed_time(e[1]) for e in ee) / 1e3
+    te_d = sum(e[1].elapsed_time(e[2]) for e in ee) / 1e3
+    h2d = 3 * q.numel() * 2
+    d2h = 2 * (o.numel() * 2 + lse.numel() * 4)
+    e2e_tflops = world * e2e_steps * (f_nc + f_c) / te_p / 1e12
+
+    # ---- CPU baseline: the oracle on the host cores, a bounded sample
+    cpu = None
+    if rank == 0 and world == 1:
+        f, s, heads = oracle_prefill_sample(wp, args.cpu_budget)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{heads} whole heads (1 head = {wp.Nq}x{wp.Nk}, d={wp.d}) of {wp.name}, "
+                         f"non-causal/causal alternating, fp64 NumPy, {s:.1f} s"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    traffic = recorded_traffic("prefill_sm103.cu", wp.name)
+    dtraffic = recorded_traffic("decode_sm103.cu", wd.name)
+    line = {
+        "metric": METRIC,
+        "value": prefill_tflops,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": (t_nc + t_c + t_d) / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{wp.name} (non-causal + causal) + {wd.name}", "B": wp.B, "H": wp.H,
+                   "Nq": wp.Nq, "Nk": wp.Nk, "d": wp.d, "scale": wp.scale, "causal": [False, True],
+                   "decode": {"B": wd.B, "H": wd.H, "Nk": wd.Nk, "d": wd.d, "num_splits": wd.num_splits},
+                   "l2": "flushed between steps (256 MB write outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"], "traffic": traffic,
+                     "kernel": "fa_prefill_kernel<64>", "peak_source": f"{peaks['source']} bf16 burst",
+                     "ms_noncausal": t_nc / K * 1e3, "ms_causal": t_c / K * 1e3},
+        "decode": {"value": decode_gbs, "unit": "GB/s", "ms": t_d / K * 1e3, "bytes": dec_bytes,
+                   "roofline": {"bound": "hbm", "achieved": K * dec_bytes / t_d / 1e9, "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": K * dec_bytes / t_d / 1e9 / peaks["hbm_gbs"],
+                                "traffic": dtraffic, "kernel": "fa_decode_split_kernel<128> + merge",
+                                "peak_source": f"{peaks['source']} copy"},
+                   "e2e": {"value": world * e2e_steps * dec_bytes / te_d / 1e9, "unit": "GB/s",
+                           "h2d_bytes_per_step": dq.numel() * 2,
+                           "d2h_bytes_per_step": do.numel() * 2 + dlse.numel() * 4,
+                           "note": "KV cache resident on the device; q in, o and lse out per step"}},
+        "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "wall_s_timed": t_wall1 - t_wall0,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

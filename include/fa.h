@@ -1,0 +1,142 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library libfa_gb300.so.
+ *
+ * The operation (all entry points): for every batch b, head h and query row i
+ *
+ *     s_ij  = scale * <q_i, k_j>                       (scaled scores)
+ *     allowed(i, j) = (!causal || j <= i + (Nk - Nq)) && keep(b, h, i, j)
+ *     O_i   = sum_j softmax_j(s_ij over allowed j) * v_j
+ *     lse_i = ln sum_{allowed j} exp(s_ij)
+ *
+ * "Flash Attention Optimization", section "Attention is not slow because of
+ * arithmetic" (S = Q K^T / sqrt(d), P = softmax(S), O = P V); "Explain
+ * FlashAttention. Why is it called IO-aware, and what does it actually
+ * save?", section "Keep only the state needed for the final weighted average"
+ * (scores plus the intended mask or bias; the causal mask uses absolute query
+ * and key positions). A row with no allowed key returns O = 0 and
+ * lse = -inf (the explicit empty-row policy of the section "Executable
+ * recurrence, with an empty-state policy"). lse is the per-row statistic a
+ * backward pass recomputes P from ("Flash Attention Optimization", section
+ * "Sizing a tile, and why the backward pass recomputes instead of storing").
+ * Causal alignment for Nq != Nk is bottom-right (query i sees keys
+ * j <= i + Nk - Nq), the reading the library takes where the pages are silent.
+ *
+ * Layout (all device pointers, row-major, contiguous):
+ *   q, o      bf16 [B, H, Nq, d]        k, v   bf16 [B, H, Nk, d]
+ *   lse       fp32 [B, H, Nq]           (may be NULL: not written)
+ *   keep_bits uint32 words; bit (j % 32) of word (j / 32) is key j, 1 = attend;
+ *             the words of row (b, h, i) start at
+ *             b*mstride_b + h*mstride_h + i*mstride_q (strides in words;
+ *             mstride_q = 0 broadcasts one key mask over all rows). Each row
+ *             holds ceil(Nk / 32) words; bits past Nk are ignored.
+ *   stream    a cudaStream_t (NULL = the legacy default stream).
+ * Supported: d in {64, 128}; q, k, v, o 16-byte aligned; keep_bits 4-byte
+ * aligned; 1 <= B*H, Nk < 2^31; scale finite and >= 0.
+ *
+ * Ownership: the caller allocates and owns every buffer; the library keeps
+ * no pointer after a call returns and allocates no device memory per call
+ * (the decode workspace is the caller's). Calls are asynchronous on `stream`:
+ * a return of FA_OK means the work was launched.
+ *
+ * Errors (checked on the host before anything is launched; nothing is
+ * written on error):
+ *   FA_ERR_INVALID_ARG  a required pointer is NULL, a size is negative or
+ *                       zero where it must be positive, scale is NaN/inf or
+ *                       negative, or a size overflows the supported range.
+ *   FA_ERR_UNSUPPORTED  d not in {64, 128}, a misaligned pointer, or no
+ *                       sm_103 device is current. There is no fallback path.
+ *   FA_ERR_WORKSPACE    the decode workspace is NULL or too small.
+ *   FA_ERR_CUDA         a CUDA call failed (fa_last_error_detail() says which).
+ *   FA_ERR_TIMEOUT      reported later by fa_get_device_status(): a bounded
+ *                       wait inside a kernel gave up; that call's outputs are
+ *                       undefined, the CUDA context stays usable.
+ * Inputs are not scanned for NaN/inf (that would cost bandwidth): a NaN or
+ * inf in q, k or v propagates to the rows it touches.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_CUDA = 3,
+  FA_ERR_TIMEOUT = 4,
+  FA_ERR_WORKSPACE = 5
+} fa_status;
+
+/* Fused, tiled forward pass (prefill). Q tiles stay on chip while K/V tiles
+ * stream through; the Nq x Nk score matrix never reaches HBM ("Flash
+ * Attention Optimization", section "The fix: tile the computation, never
+ * materialize the full matrix"). Nq = 0 is a no-op. */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int Nq, int Nk, int d, float scale, int causal, void* stream);
+
+/* fa_fwd with an additional key mask (see keep_bits above), ANDed with the
+ * causal mask when causal != 0. keep_bits = NULL is the same as fa_fwd. */
+fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                        const uint32_t* keep_bits, int64_t mstride_b, int64_t mstride_h,
+                        int64_t mstride_q, void* stream);
+
+/* Bytes of device workspace fa_decode_splitkv needs: fp32 partial
+ * (o[d], m, l) per (b, h, split), i.e. B*H*num_splits*(d + 2)*4 rounded up
+ * to 256. Returns 0 for invalid arguments. */
+size_t fa_decode_workspace_size(int B, int H, int d, int num_splits);
+
+/* Split-KV decode: one query token per (b, h) against a KV cache of Nk keys
+ * ("FlashAttention: Attention Is Limited by Memory, Not Math", section
+ * "Where it helps, and where it does not": split the K/V sequence across the
+ * GPU, then merge the partial results; the merge re-bases each split to the
+ * global max, "Handwritten Notes on Flash Attention", section "Merging two
+ * blocks"). Split s covers keys [s*c, min(Nk, (s+1)*c)) with
+ * c = ceil(Nk / num_splits); empty splits contribute nothing.
+ *   q, o     bf16 [B, H, 1, d]     k_cache, v_cache  bf16 [B, H, Nk, d]
+ *   lse      fp32 [B, H] (may be NULL)
+ *   workspace  device memory of at least fa_decode_workspace_size() bytes,
+ *              256-byte aligned, owned by the caller; its contents on entry
+ *              do not matter and are overwritten.
+ *   1 <= num_splits <= 1024. Two launches (split, then merge) on `stream`. */
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                            int B, int H, int Nk, int d, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device: FA_ERR_TIMEOUT if a bounded wait gave up since the
+ * last call, FA_ERR_CUDA if the stream reported an error, else FA_OK. */
+fa_status fa_get_device_status(void* stream);
+
+/* Limit, in nanoseconds, on every wait inside the library's kernels
+ * (default 2e9). Applies to calls launched afterwards. */
+void fa_set_wait_limit_ns(uint64_t ns);
+uint64_t fa_get_wait_limit_ns(void);
+
+/* Self-test of the failure path: launches one warp that waits on a barrier
+ * nothing ever arrives on, with the given limit; returns what
+ * fa_get_device_status() then reports (FA_ERR_TIMEOUT when the bounded wait
+ * works). The context stays usable afterwards. */
+fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Human-readable name of a status code. */
+const char* fa_status_string(fa_status s);
+
+/* Detail of the most recent error returned on the calling host thread
+ * (empty string if none). */
+const char* fa_last_error_detail(void);
+
+/* Number of kernel launches this library issued on the calling host thread
+ * since the process started (for accounting in benchmarks). */
+uint64_t fa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,270 @@
+// Host side of the C ABI declared in include/fa.h: argument validation,
+// TMA descriptor encoding, launch configuration and the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_common.cuh"
+
+namespace fa {
+// One status word per device; kernels atomicOr FA_DEV_* bits into it.
+__device__ unsigned int g_device_status = 0u;
+}  // namespace fa
+
+namespace {
+
+thread_local char t_detail[512] = {0};
+thread_local uint64_t t_launches = 0;
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_detail, sizeof(t_detail), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceState {
+  bool ready = false;
+  unsigned int* status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device one-time set-up: device check, status-word address, kernel
+// attributes, driver entry point for tensor-map encoding.
+fa_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+    if (major != 10 || minor != 3)
+      return fail(FA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                  minor);
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, fa::g_device_status)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    st.status = static_cast<unsigned int*>(p);
+    if ((e = fa::prefill_set_attributes(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
+    if ((e = fa::prefill_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
+    // The in-kernel register split assumes this launch allocation; a
+    // different one could make setmaxnreg.inc wait forever, so refuse.
+    for (int d : {64, 128}) {
+      const int regs = fa::prefill_num_regs(d);
+      if (regs != fa::PREFILL_LAUNCH_REGS)
+        return fail(FA_ERR_UNSUPPORTED, "prefill kernel (d=%d) built with %d registers, expected %d", d, regs,
+                    fa::PREFILL_LAUNCH_REGS);
+    }
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(FA_ERR_CUDA, "driver entry point cuTensorMapEncodeTiled unavailable");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.ready = true;
+  }
+  *out = &st;
+  return FA_OK;
+}
+
+// 3-D bf16 tensor map over [BH, rows, d] with 128-row x 64-column boxes and
+// 128-byte swizzle; rows past `rows` read as zeros.
+fa_status encode_map(CUtensorMap* map, const void* base, int rows, int BH, int d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+  return FA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fa_status check_scale(float scale) {
+  if (!std::isfinite(scale) || scale < 0.f) return fail(FA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+  }
+  return "FA_UNKNOWN_STATUS";
+}
+
+const char* fa_last_error_detail(void) { return t_detail; }
+
+uint64_t fa_launch_count(void) { return t_launches; }
+
+void fa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
+uint64_t fa_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
+
+fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                        int Nk, int d, float scale, int causal, const uint32_t* keep_bits, int64_t mstride_b,
+                        int64_t mstride_h, int64_t mstride_q, void* stream) {
+  t_detail[0] = 0;
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  if (B < 1 || H < 1 || Nk < 1 || Nq < 0)
+    return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Nk >= 1, Nq >= 0 (got %d %d %d %d)", B, H, Nk, Nq);
+  if (fa_status s = check_scale(scale)) return s;
+  if (mstride_b < 0 || mstride_h < 0 || mstride_q < 0) return fail(FA_ERR_INVALID_ARG, "mask strides must be >= 0");
+  const long long BH = static_cast<long long>(B) * H;
+  const long long n_qpairs = (static_cast<long long>(Nq) + 2 * fa::BLOCK_M - 1) / (2 * fa::BLOCK_M);
+  if (BH > INT_MAX || n_qpairs * BH > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B*H or the grid is too large");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(FA_ERR_UNSUPPORTED, "q, k, v, o must be 16-byte aligned");
+  if (keep_bits && !aligned(keep_bits, 4)) return fail(FA_ERR_UNSUPPORTED, "keep_bits must be 4-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(FA_ERR_UNSUPPORTED, "lse must be 4-byte aligned");
+  if (Nq == 0) return FA_OK;
+
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  CUtensorMap tq, tk, tv;
+  if (fa_status s = encode_map(&tq, q, Nq, static_cast<int>(BH), d)) return s;
+  if (fa_status s = encode_map(&tk, k, Nk, static_cast<int>(BH), d)) return s;
+  if (fa_status s = encode_map(&tv, v, Nk, static_cast<int>(BH), d)) return s;
+
+  fa::PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.keep = keep_bits;
+  p.msb = mstride_b;
+  p.msh = mstride_h;
+  p.msq = mstride_q;
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qpairs = static_cast<int>(n_qpairs);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.status = st->status;
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  t_launches += 1;
+  return FA_OK;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                 int d, float scale, int causal, void* stream) {
+  return fa_fwd_masked(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, nullptr, 0, 0, 0, stream);
+}
+
+size_t fa_decode_workspace_size(int B, int H, int d, int num_splits) {
+  if (B < 1 || H < 1 || (d != 64 && d != 128) || num_splits < 1 || num_splits > 1024) return 0;
+  const size_t parts = static_cast<size_t>(B) * H * num_splits;
+  const size_t o_bytes = (parts * d * 4 + 255) & ~size_t(255);
+  const size_t ml_bytes = (parts * 2 * 4 + 255) & ~size_t(255);
+  return o_bytes + ml_bytes;
+}
+
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B,
+                            int H, int Nk, int d, float scale, int num_splits, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  t_detail[0] = 0;
+  if (!q || !k_cache || !v_cache || !o) return fail(FA_ERR_INVALID_ARG, "q, k_cache, v_cache and o must be non-NULL");
+  if (B < 1 || H < 1 || Nk < 1) return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Nk >= 1");
+  if (num_splits < 1 || num_splits > 1024) return fail(FA_ERR_INVALID_ARG, "num_splits must be in [1, 1024]");
+  if (fa_status s = check_scale(scale)) return s;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH * num_splits > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B*H*num_splits is too large");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16))
+    return fail(FA_ERR_UNSUPPORTED, "q, k_cache, v_cache, o must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(FA_ERR_UNSUPPORTED, "lse must be 4-byte aligned");
+  const size_t need = fa_decode_workspace_size(B, H, d, num_splits);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", need);
+
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  const size_t parts = static_cast<size_t>(BH) * num_splits;
+  fa::DecodeParams p{};
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.o = o;
+  p.lse = lse;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((parts * d * 4 + 255) & ~size_t(255)));
+  p.BH = static_cast<int>(BH);
+  p.Nk = Nk;
+  p.S = num_splits;
+  p.chunk = (Nk + num_splits - 1) / num_splits;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e = fa::launch_decode(d, p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  t_launches += 2;
+  return FA_OK;
+}
+
+fa_status fa_get_device_status(void* stream) {
+  t_detail[0] = 0;
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  if ((e = cudaMemcpyAsync(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "read status");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (word != 0u) {
+    if ((e = cudaMemsetAsync(st->status, 0, sizeof(word), s)) != cudaSuccess) return cuda_fail(e, "clear status");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  }
+  if (word & fa::FA_DEV_TIMEOUT) return fail(FA_ERR_TIMEOUT, "a bounded wait inside a kernel gave up");
+  return FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  t_detail[0] = 0;
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  cudaError_t e = fa::launch_wait_selftest(limit_ns, st->status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  t_launches += 1;
+  return fa_get_device_status(stream);
+}
+
+}  // extern "C"

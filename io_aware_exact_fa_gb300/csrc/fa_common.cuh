@@ -1,0 +1,63 @@
+// Definitions shared by the kernels and the host side of the C-ABI library.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Bits of the device status word (one word per device, cleared by
+// fa_get_device_status).
+constexpr unsigned int FA_DEV_TIMEOUT = 1u;   // a bounded wait ran out
+
+// Prefill tiling: 128 query rows per Q tile, two Q tiles per CTA, 128 keys per
+// K/V tile.
+constexpr int BLOCK_M = 128;
+constexpr int BLOCK_N = 128;
+constexpr int Q_TILES = 2;
+constexpr int PREFILL_THREADS = 384;   // 2 softmax warpgroups + 1 producer warpgroup (TMA, MMA, 2 idle)
+// Register split after set-up (setmaxnreg): the launch gives every thread
+// PREFILL_LAUNCH_REGS; per SM sub-partition one warp of each warpgroup, so
+// 2 * SOFTMAX + PRODUCER must not exceed 3 * PREFILL_LAUNCH_REGS.
+constexpr int PREFILL_LAUNCH_REGS = 168;
+constexpr int PREFILL_SOFTMAX_REGS = 232;
+constexpr int PREFILL_PRODUCER_REGS = 40;
+static_assert(2 * PREFILL_SOFTMAX_REGS + PREFILL_PRODUCER_REGS <= 3 * PREFILL_LAUNCH_REGS,
+              "setmaxnreg split exceeds the registers the launch provides");
+
+struct PrefillParams {
+  void* o;                   // bf16 [B*H, Nq, d]
+  float* lse;                // fp32 [B*H, Nq] or nullptr
+  const uint32_t* keep;      // packed key mask or nullptr
+  int64_t msb, msh, msq;     // mask strides in 32-bit words
+  int B, H, Nq, Nk;
+  int n_qpairs;              // ceil(Nq / 256)
+  int causal;
+  float scale_log2;          // scale * log2(e)
+  uint64_t wait_limit_ns;
+  unsigned int* status;      // device status word
+};
+
+struct DecodeParams {
+  const void* q;             // bf16 [B*H, d]
+  const void* k;             // bf16 [B*H, Nk, d]
+  const void* v;             // bf16 [B*H, Nk, d]
+  void* o;                   // bf16 [B*H, d]
+  float* lse;                // fp32 [B*H] or nullptr
+  float* ws_o;               // fp32 [B*H, S, d]   unnormalised partial outputs
+  float* ws_ml;              // fp32 [B*H, S, 2]   partial (max in log2 units, sum)
+  int BH, Nk, S, chunk;
+  float scale_log2;
+};
+
+// Launchers (defined next to their kernels). Return a CUDA error code.
+cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, cudaStream_t stream);
+size_t prefill_smem_bytes(int d);
+cudaError_t prefill_set_attributes(int d);
+int prefill_num_regs(int d);   // registers per thread the prefill kernel launches with
+cudaError_t launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int* status, cudaStream_t stream);
+
+}  // namespace fa

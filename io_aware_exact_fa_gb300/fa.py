@@ -1,0 +1,184 @@
+"""Thin ctypes binding over libfa_gb300.so (include/fa.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels. PyTorch supplies device memory and the current
+stream. Importing this module raises ImportError when the library has not
+been built (there is no fallback path).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m io_aware_exact_fa_gb300.build` "
+        "(or __graft_entry__.build()); there is no non-CUDA fallback")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_u64 = ctypes.c_uint64
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_WORKSPACE = range(6)
+
+EXPORTS = {
+    "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i64, _i64, _i64, _vp]),
+    "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_decode_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
+    "fa_get_device_status": (_i, [_vp]),
+    "fa_set_wait_limit_ns": (None, [_u64]),
+    "fa_get_wait_limit_ns": (_u64, []),
+    "fa_selftest_wait_timeout": (_i, [_u64, _vp]),
+    "fa_status_string": (ctypes.c_char_p, [_i]),
+    "fa_last_error_detail": (ctypes.c_char_p, []),
+    "fa_launch_count": (_u64, []),
+}
+for _name, (_res, _args) in EXPORTS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        detail = _lib.fa_last_error_detail().decode()
+        super().__init__(f"{where}: {_lib.fa_status_string(status).decode()} {detail}".strip())
+
+
+def _check(status: int, where: str) -> None:
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+        causal: bool = False, keep_bits: Optional[torch.Tensor] = None,
+        mask_strides: Tuple[int, int, int] = (0, 0, 0), out: Optional[torch.Tensor] = None,
+        lse: Optional[torch.Tensor] = None, with_lse: bool = True,
+        stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Exact attention forward pass: q [B,H,Nq,d], k/v [B,H,Nk,d] bf16 -> (o bf16, lse fp32).
+
+    ``keep_bits`` (int32 words, bit j%32 of word j//32 = key j, 1 = attend)
+    with ``mask_strides`` = (b, h, q) strides in words; q stride 0 broadcasts.
+    """
+    _need(q, "q"); _need(k, "k"); _need(v, "v")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out")
+    if with_lse and lse is None:
+        lse = torch.empty(B, H, Nq, dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    st = _stream_ptr(stream)
+    lp = lse.data_ptr() if lse is not None else None
+    if keep_bits is None:
+        rc = _lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lp,
+                         B, H, Nq, Nk, d, float(scale), int(bool(causal)), st)
+        _check(rc, "fa_fwd")
+    else:
+        _need(keep_bits, "keep_bits", torch.int32)
+        sb, sh, sq = mask_strides
+        rc = _lib.fa_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lp,
+                                B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+                                keep_bits.data_ptr(), int(sb), int(sh), int(sq), st)
+        _check(rc, "fa_fwd_masked")
+    return out, lse
+
+
+def decode_workspace_size(B: int, H: int, d: int, num_splits: int) -> int:
+    return int(_lib.fa_decode_workspace_size(B, H, d, num_splits))
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, scale: Optional[float] = None,
+           num_splits: int = 16, workspace: Optional[torch.Tensor] = None,
+           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, with_lse: bool = True,
+           stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Split-KV decode: q [B,H,1,d], caches [B,H,Nk,d] bf16 -> (o [B,H,1,d] bf16, lse [B,H] fp32)."""
+    _need(q, "q"); _need(k_cache, "k_cache"); _need(v_cache, "v_cache")
+    B, H, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query token per (b, h): q must be [B, H, 1, d]")
+    Nk = k_cache.shape[2]
+    if k_cache.shape != (B, H, Nk, d) or v_cache.shape != (B, H, Nk, d):
+        raise ValueError("k_cache and v_cache must be [B, H, Nk, d]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = decode_workspace_size(B, H, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out")
+    if with_lse and lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    rc = _lib.fa_decode_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                lse.data_ptr() if lse is not None else None, B, H, Nk, d, float(scale),
+                                int(num_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_ptr(stream))
+    _check(rc, "fa_decode_splitkv")
+    return out, lse
+
+
+def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronise and return (then clear) the library's device status (FA_OK or FA_ERR_TIMEOUT)."""
+    return int(_lib.fa_get_device_status(_stream_ptr(stream)))
+
+
+def selftest_wait_timeout(limit_ns: int, stream: Optional[torch.cuda.Stream] = None) -> int:
+    return int(_lib.fa_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _lib.fa_set_wait_limit_ns(int(ns))
+
+
+def get_wait_limit_ns() -> int:
+    return int(_lib.fa_get_wait_limit_ns())
+
+
+def launch_count() -> int:
+    return int(_lib.fa_launch_count())
+
+
+def status_string(s: int) -> str:
+    return _lib.fa_status_string(s).decode()
+
+
+# raw handle for callers that pass their own pointers (host-buffer end-to-end timing, tests)
+lib = _lib
