@@ -159,7 +159,7 @@ def oracle_prefill_sample(w, budget_s: float):
         flops += per_head / 2 if causal else per_head
         heads += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or heads >= 64:
+        if el >= budget_s or heads >= 4096:
             return flops, el, heads
 
 
@@ -203,7 +203,12 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for cpu_baseline (0 = skip)")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                    help="run one part of the step only (small profiling runs)")
+    ap.add_argument("--decode-b", type=int, default=0, help="override the decode batch (profiling a small case)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -223,15 +228,23 @@ def main():
     B.build()
     from io_aware_exact_fa_gb300 import fa, workloads as W
 
+    do_p = args.only in ("all", "prefill")
+    do_d = args.only in ("all", "decode")
     wp = W.WORKLOADS[PREFILL]
     wd = W.WORKLOADS[DECODE]
-    q, k, v = W.make_qkv(wp.B, wp.H, wp.Nq, wp.Nk, wp.d, seed=rank, device="cuda")
-    o = torch.empty_like(q)
-    lse = torch.empty(wp.B, wp.H, wp.Nq, dtype=torch.float32, device=dev)
-    dq, dk, dv = W.make_qkv(wd.B, wd.H, 1, wd.Nk, wd.d, seed=1000 + rank, device="cuda")
-    do = torch.empty_like(dq)
-    dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
-    ws = torch.empty(fa.decode_workspace_size(wd.B, wd.H, wd.d, wd.num_splits), dtype=torch.uint8, device=dev)
+    if args.decode_b:
+        import dataclasses
+        wd = dataclasses.replace(wd, B=args.decode_b, name=wd.name.replace("b64", f"b{args.decode_b}"))
+    if do_p:
+        q, k, v = W.make_qkv(wp.B, wp.H, wp.Nq, wp.Nk, wp.d, seed=rank, device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty(wp.B, wp.H, wp.Nq, dtype=torch.float32, device=dev)
+    if do_d:
+        dq, dk, dv = W.make_qkv(wd.B, wd.H, 1, wd.Nk, wd.d, seed=1000 + rank, device="cuda")
+        do = torch.empty_like(dq)
+        dlse = torch.empty(wd.B, wd.H, dtype=torch.float32, device=dev)
+        ws = torch.empty(fa.decode_workspace_size(wd.B, wd.H, wd.d, wd.num_splits), dtype=torch.uint8,
+                         device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -241,16 +254,32 @@ def main():
     def decode():
         fa.decode(dq, dk, dv, scale=wd.scale, num_splits=wd.num_splits, workspace=ws, out=do, lse=dlse)
 
-    for _ in range(max(3, args.warmup)):
+    def step_body(e):
+        e[0].record(stream)
+        if do_p:
+            prefill(False)
+        e[1].record(stream)
+        if do_p:
+            prefill(True)
+        e[2].record(stream)
+        if do_d:
+            decode()
+        e[3].record(stream)
+
+    warm = max(3, args.warmup)
+    for _ in range(warm):
         flush.zero_()
-        prefill(False)
-        prefill(True)
-        decode()
+        if do_p:
+            prefill(False)
+            prefill(True)
+        if do_d:
+            decode()
     torch.cuda.synchronize()
     if fa.device_status() != fa.FA_OK:
         raise RuntimeError("device status not OK after warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.2)
@@ -259,16 +288,9 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for i in range(args.steps):
+    for i in range(K):
         flush.zero_()                     # outside the events: evicts the prefill inputs from L2
-        e = ev[i]
-        e[0].record(stream)
-        prefill(False)
-        e[1].record(stream)
-        prefill(True)
-        e[2].record(stream)
-        decode()
-        e[3].record(stream)
+        step_body(ev[i])
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -286,54 +308,56 @@ def main():
     if world > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
     t_nc, t_c, t_d = times.tolist()
-    K = args.steps
     f_nc, f_c = wp.flops(False), wp.flops(True)
-    prefill_tflops = world * K * (f_nc + f_c) / (t_nc + t_c) / 1e12
-    kernel_tflops = K * (f_nc + f_c) / (t_nc + t_c) / 1e12          # per launch average, this GPU
-    dec_bytes = wd.io_bytes()
-    decode_gbs = world * K * dec_bytes / t_d / 1e9
     peaks = measured_peaks()
+    dec_bytes = wd.io_bytes()
 
     # ---- end to end through the public API with pinned host buffers
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    ho2 = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hl2 = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    hdq = dq.cpu().pin_memory()
-    hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
-    hdl = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
-    e2e_steps = max(3, min(K, 20))
-    torch.cuda.synchronize()
-    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_steps)]
-    for i in range(e2e_steps):
-        flush.zero_()
-        ee[i][0].record(stream)
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        prefill(False)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-        prefill(True)
-        ho2.copy_(o, non_blocking=True)
-        hl2.copy_(lse, non_blocking=True)
-        ee[i][1].record(stream)
-        dq.copy_(hdq, non_blocking=True)
-        decode()
-        hdo.copy_(do, non_blocking=True)
-        hdl.copy_(dlse, non_blocking=True)
-        ee[i][2].record(stream)
-    torch.cuda.synchronize()
-    te_p = sum(e[0].elapsed_time(e[1]) for e in ee) / 1e3
-    te_d = sum(e[1].elapsed_time(e[2]) for e in ee) / 1e3
-    h2d = 3 * q.numel() * 2
-    d2h = 2 * (o.numel() * 2 + lse.numel() * 4)
-    e2e_tflops = world * e2e_steps * (f_nc + f_c) / te_p / 1e12
+    e2e = dec_e2e = None
+    if not args.no_e2e:
+        n_e = max(3, min(K, 20))
+        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_e)]
+        if do_p:
+            hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+            ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+            hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
+        if do_d:
+            hdq = dq.cpu().pin_memory()
+            hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
+            hdl = torch.empty(dlse.shape, dtype=dlse.dtype).pin_memory()
+        torch.cuda.synchronize()
+        for i in range(n_e):
+            flush.zero_()
+            ee[i][0].record(stream)
+            if do_p:
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                for c, causal in enumerate((False, True)):
+                    prefill(causal)
+                    ho[c].copy_(o, non_blocking=True)
+                    hl[c].copy_(lse, non_blocking=True)
+            ee[i][1].record(stream)
+            if do_d:
+                dq.copy_(hdq, non_blocking=True)
+                decode()
+                hdo.copy_(do, non_blocking=True)
+                hdl.copy_(dlse, non_blocking=True)
+            ee[i][2].record(stream)
+        torch.cuda.synchronize()
+        te_p = sum(e[0].elapsed_time(e[1]) for e in ee) / 1e3
+        te_d = sum(e[1].elapsed_time(e[2]) for e in ee) / 1e3
+        if do_p:
+            e2e = {"value": world * n_e * (f_nc + f_c) / te_p / 1e12, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": 2 * (o.numel() * 2 + lse.numel() * 4)}
+        if do_d:
+            dec_e2e = {"value": world * n_e * dec_bytes / te_d / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": dq.numel() * 2, "d2h_bytes_per_step": do.numel() * 2 + dlse.numel() * 4,
+                       "note": "KV cache resident on the device; q in, o and lse out per step"}
 
     # ---- CPU baseline: the oracle on the host cores, a bounded sample
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_budget > 0 and do_p:
         f, s, heads = oracle_prefill_sample(wp, args.cpu_budget)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{heads} whole heads (1 head = {wp.Nq}x{wp.Nk}, d={wp.d}) of {wp.name}, "
@@ -343,45 +367,51 @@ def main():
         if world > 1:
             dist.destroy_process_group()
         return 0
-    traffic = recorded_traffic("prefill_sm103.cu", wp.name)
-    dtraffic = recorded_traffic("decode_sm103.cu", wd.name)
     line = {
         "metric": METRIC,
-        "value": prefill_tflops,
+        "value": world * K * (f_nc + f_c) / (t_nc + t_c) / 1e12 if do_p else None,
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": K,
-        "warmup": max(3, args.warmup),
+        "warmup": warm,
         "ms_per_step": (t_nc + t_c + t_d) / K * 1e3,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{wp.name} (non-causal + causal) + {wd.name}", "B": wp.B, "H": wp.H,
-                   "Nq": wp.Nq, "Nk": wp.Nk, "d": wp.d, "scale": wp.scale, "causal": [False, True],
+        "config": {"workload": (f"{wp.name} (non-causal + causal)" if do_p else "")
+                   + (" + " if do_p and do_d else "") + (wd.name if do_d else ""),
+                   "B": wp.B, "H": wp.H, "Nq": wp.Nq, "Nk": wp.Nk, "d": wp.d, "scale": wp.scale,
+                   "causal": [False, True],
                    "decode": {"B": wd.B, "H": wd.H, "Nk": wd.Nk, "d": wd.d, "num_splits": wd.num_splits},
                    "l2": "flushed between steps (256 MB write outside the timed events)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": kernel_tflops / peaks["bf16_tflops"], "traffic": traffic,
-                     "kernel": "fa_prefill_kernel<64>", "peak_source": f"{peaks['source']} bf16 burst",
-                     "ms_noncausal": t_nc / K * 1e3, "ms_causal": t_c / K * 1e3},
-        "decode": {"value": decode_gbs, "unit": "GB/s", "ms": t_d / K * 1e3, "bytes": dec_bytes,
-                   "roofline": {"bound": "hbm", "achieved": K * dec_bytes / t_d / 1e9, "peak": peaks["hbm_gbs"],
-                                "unit": "GB/s", "frac": K * dec_bytes / t_d / 1e9 / peaks["hbm_gbs"],
-                                "traffic": dtraffic, "kernel": "fa_decode_split_kernel<128> + merge",
-                                "peak_source": f"{peaks['source']} copy"},
-                   "e2e": {"value": world * e2e_steps * dec_bytes / te_d / 1e9, "unit": "GB/s",
-                           "h2d_bytes_per_step": dq.numel() * 2,
-                           "d2h_bytes_per_step": do.numel() * 2 + dlse.numel() * 4,
-                           "note": "KV cache resident on the device; q in, o and lse out per step"}},
-        "e2e": {"value": e2e_tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": launches,
         "cpu_baseline": cpu,
         "clocks": clocks,
         "wall_s_timed": t_wall1 - t_wall0,
     }
+    if do_p:
+        ach = K * (f_nc + f_c) / (t_nc + t_c) / 1e12
+        line["roofline"] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": ach / peaks["bf16_tflops"],
+                            "traffic": recorded_traffic("prefill_sm103.cu", wp.name),
+                            "kernel": "fa_prefill_kernel<64>", "peak_source": f"{peaks['source']} bf16 burst",
+                            "ms_noncausal": t_nc / K * 1e3, "ms_causal": t_c / K * 1e3,
+                            "tflops_noncausal": K * f_nc / t_nc / 1e12, "tflops_causal": K * f_c / t_c / 1e12}
+    if do_d:
+        ach = K * dec_bytes / t_d / 1e9
+        line["decode"] = {"value": world * ach, "unit": "GB/s", "ms": t_d / K * 1e3, "bytes": dec_bytes,
+                          "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                       "frac": ach / peaks["hbm_gbs"],
+                                       "traffic": recorded_traffic("decode_sm103.cu", wd.name),
+                                       "kernel": "fa_decode_split_kernel<128> + fa_decode_merge_kernel<128>",
+                                       "peak_source": f"{peaks['source']} copy"},
+                          "e2e": dec_e2e}
+        if not do_p:
+            line["value"], line["unit"] = line["decode"]["value"], "GB/s"
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

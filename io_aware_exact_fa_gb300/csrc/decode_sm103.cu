@@ -220,6 +220,24 @@ __global__ void fa_wait_selftest_kernel(uint64_t limit_ns, unsigned int* status)
   __syncthreads();
 }
 
+// Evaluates the FMA-pipe exponential used by the prefill softmax on n inputs.
+__global__ void fa_exp2_selftest_kernel(const float* x, float* y, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x0 = x[i];
+  const float x1 = (i + 1 < n) ? x[i + 1] : 0.f;
+  float y0, y1;
+  f2unpack(exp2_fma2(f2pack(x0, x1)), y0, y1);
+  y[i] = y0;
+  if (i + 1 < n) y[i + 1] = y1;
+}
+
+cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream) {
+  const int pairs = (n + 1) / 2;
+  fa_exp2_selftest_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int* status, cudaStream_t stream) {
   fa_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
   return cudaGetLastError();

@@ -141,20 +141,20 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
                         int Nk, int d, float scale, int causal, const uint32_t* keep_bits, int64_t mstride_b,
                         int64_t mstride_h, int64_t mstride_q, void* stream) {
   t_detail[0] = 0;
-  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
   if (B < 1 || H < 1 || Nk < 1 || Nq < 0)
     return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Nk >= 1, Nq >= 0 (got %d %d %d %d)", B, H, Nk, Nq);
   if (fa_status s = check_scale(scale)) return s;
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
+  if (Nq == 0) return FA_OK;  // nothing to compute (an empty q may have a NULL data pointer)
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
   if (mstride_b < 0 || mstride_h < 0 || mstride_q < 0) return fail(FA_ERR_INVALID_ARG, "mask strides must be >= 0");
   const long long BH = static_cast<long long>(B) * H;
   const long long n_qpairs = (static_cast<long long>(Nq) + 2 * fa::BLOCK_M - 1) / (2 * fa::BLOCK_M);
   if (BH > INT_MAX || n_qpairs * BH > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B*H or the grid is too large");
-  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
     return fail(FA_ERR_UNSUPPORTED, "q, k, v, o must be 16-byte aligned");
   if (keep_bits && !aligned(keep_bits, 4)) return fail(FA_ERR_UNSUPPORTED, "keep_bits must be 4-byte aligned");
   if (lse && !aligned(lse, 4)) return fail(FA_ERR_UNSUPPORTED, "lse must be 4-byte aligned");
-  if (Nq == 0) return FA_OK;
 
   DeviceState* st = nullptr;
   if (fa_status s = device_state(&st)) return s;
@@ -176,7 +176,10 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
   p.Nk = Nk;
   p.n_qpairs = static_cast<int>(n_qpairs);
   p.causal = causal ? 1 : 0;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // scale 0 (uniform weights) runs with the smallest normal multiplier instead,
+  // so masked scores (-inf) still map to -inf and exponentiate to exactly 0;
+  // every weight then differs from 1 by far less than fp32 resolution.
+  p.scale_log2 = fmaxf(scale * 1.4426950408889634f, 1.17549435e-38f);
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
   cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
@@ -265,6 +268,18 @@ fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   t_launches += 1;
   return fa_get_device_status(stream);
+}
+
+fa_status fa_selftest_exp2(const float* x, float* y, int n, void* stream) {
+  t_detail[0] = 0;
+  if (n < 0 || (n > 0 && (!x || !y))) return fail(FA_ERR_INVALID_ARG, "need n >= 0 and non-NULL x, y");
+  if (n == 0) return FA_OK;
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  cudaError_t e = fa::launch_exp2_selftest(x, y, n, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "exp2 self-test launch");
+  t_launches += 1;
+  return FA_OK;
 }
 
 }  // extern "C"

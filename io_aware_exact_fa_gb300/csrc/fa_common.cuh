@@ -21,8 +21,8 @@ constexpr int PREFILL_THREADS = 384;   // 2 softmax warpgroups + 1 producer warp
 // PREFILL_LAUNCH_REGS; per SM sub-partition one warp of each warpgroup, so
 // 2 * SOFTMAX + PRODUCER must not exceed 3 * PREFILL_LAUNCH_REGS.
 constexpr int PREFILL_LAUNCH_REGS = 168;
-constexpr int PREFILL_SOFTMAX_REGS = 232;
-constexpr int PREFILL_PRODUCER_REGS = 40;
+constexpr int PREFILL_SOFTMAX_REGS = 224;
+constexpr int PREFILL_PRODUCER_REGS = 56;
 static_assert(2 * PREFILL_SOFTMAX_REGS + PREFILL_PRODUCER_REGS <= 3 * PREFILL_LAUNCH_REGS,
               "setmaxnreg split exceeds the registers the launch provides");
 
@@ -59,5 +59,6 @@ cudaError_t prefill_set_attributes(int d);
 int prefill_num_regs(int d);   // registers per thread the prefill kernel launches with
 cudaError_t launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int* status, cudaStream_t stream);
+cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream);
 
 }  // namespace fa

@@ -228,6 +228,68 @@ __device__ __forceinline__ float lg2_approx(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Packed fp32x2 arithmetic (two lanes per 64-bit register pair).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Three-input maximum.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x on the FMA pipe for two lanes at once, for x in [-125, 127] (smaller x
+// is clamped to -125, keeping 2^j a normal number). x = j + f with j = round(x) and f in [-1/2, 1/2];
+// 2^f comes from a degree-3 polynomial whose coefficients are this library's
+// own minimax fit of the relative error on [-1/2, 1/2] (a linear program on
+// 4001 Chebyshev-spaced points; max relative error 7.5e-5 when evaluated in
+// fp32), and 2^j is applied by adding j to the exponent field. The rounding
+// uses the 1.5 * 2^23 shifter: after x + 1.5*2^23 the integer j sits in the
+// low mantissa bits.
+__device__ __forceinline__ uint64_t exp2_fma2(uint64_t x) {
+  constexpr float kShift = 12582912.0f;
+  float x0, x1;
+  f2unpack(x, x0, x1);
+  x = f2pack(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
+  const uint64_t sh = f2pack(kShift, kShift);
+  const uint64_t t = fadd2(x, sh);                    // j in the low bits
+  const uint64_t j = fadd2(t, f2pack(-kShift, -kShift));
+  float j0, j1;
+  f2unpack(j, j0, j1);
+  const uint64_t f = fadd2(x, f2pack(-j0, -j1));      // f = x - j in [-1/2, 1/2]
+  uint64_t p = ffma2(f2pack(0.05517132207751274f, 0.05517132207751274f), f,
+                     f2pack(0.2426113337278366f, 0.2426113337278366f));
+  p = ffma2(p, f, f2pack(0.6932610869407654f, 0.6932610869407654f));
+  p = ffma2(p, f, f2pack(0.9999280571937561f, 0.9999280571937561f));
+  float p0, p1, t0, t1;
+  f2unpack(p, p0, p1);
+  f2unpack(t, t0, t1);
+  const float r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
+  const float r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
+  return f2pack(r0, r1);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -16,9 +16,9 @@
 // 384 threads = 3 warpgroups; after set-up the softmax warpgroups take more
 // registers and the producer warpgroup fewer (setmaxnreg).
 //   warp 8      TMA producer: Q once, then K_j / V_j into a ring of slots.
-//   warps 10-11 idle after set-up.
-//   warp 9      TMEM allocator and MMA issuer (one thread):
+//   warp 9      TMEM allocator; with warp 10, MMA issuers (one per Q tile):
 //               S_t = Q_t K_j^T into TMEM, later O_t += P_t V_j.
+//   warp 11     idle after set-up.
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: each thread
 //               owns one query row (TMEM lane), reads its 128 scores with
 //               tcgen05.ld, applies the mask from absolute positions, folds
@@ -44,12 +44,24 @@ struct PrefillCfg {
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = Q_TILES * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
-  static constexpr int NBAR = 1 + 2 * NSLOT + 3 * Q_TILES + 1;
+  // TMEM columns: S_0 [0,128), S_1 [128,256), O_t at O_COL + D*t; with
+  // SEP_P (d = 64) P_t gets its own 64 columns at P_COL + 64*t, otherwise P_t
+  // overwrites the first 64 columns of S_t.
+  static constexpr bool SEP_P = (D == 64);
+  static constexpr uint32_t O_COL = 2 * BLOCK_N;
+  static constexpr uint32_t P_COL = SEP_P ? O_COL + Q_TILES * D : 0;
+  static constexpr uint32_t P_STRIDE = SEP_P ? BLOCK_N / 2 : BLOCK_N;
+  static_assert(!SEP_P || P_COL + Q_TILES * BLOCK_N / 2 <= 512, "TMEM budget");
+  static constexpr int NBAR = 1 + 2 * NSLOT + 4 * Q_TILES + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false);  // Q, K both K-major
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);     // V is MN-major
+  // Softmax tuning: exponential pairs (of 16 per 32 columns) computed on the
+  // FMA pipe instead of the MUFU unit, and the lazy-rescale threshold.
+  static constexpr int EMU_PAIRS = 0;
+  static constexpr float RESCALE_LOG2 = 8.0f;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -63,6 +75,58 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
     if (mbar_try_wait(a, parity)) return;
     if ((i & 31u) == 31u && globaltimer_ns() - t0 > limit_ns) return;
   }
+}
+
+// One query row's scores s[0..127] (fp32 bit patterns, masked ones -inf) ->
+// P = 2^(s * sl2 - m) as 64 bf16 pairs in pk_all, returning the row sum of
+// the fp32 exponentials. EMU pairs of every 16
+// use the FMA-pipe exponential. With MASKED, -inf scores give exactly 0 on
+// both exponential paths.
+template <bool MASKED, int EMU>
+__device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x2, uint64_t nm2, uint32_t* pk_all) {
+  uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int ch = 0; ch < BLOCK_N / 32; ++ch) {
+    uint32_t* pk = pk_all + ch * 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = ch * 32 + 2 * i;
+      const uint64_t x2 = ffma2(f2pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nm2);
+      uint64_t p2;
+      if (i >= 16 - EMU) {
+        p2 = exp2_fma2(x2);
+        if (MASKED) {
+          float p0, p1;
+          f2unpack(p2, p0, p1);
+          p0 = (s[c] == 0xff800000u) ? 0.f : p0;
+          p1 = (s[c + 1] == 0xff800000u) ? 0.f : p1;
+          p2 = f2pack(p0, p1);
+        }
+      } else {
+        float x0, x1;
+        f2unpack(x2, x0, x1);
+        p2 = f2pack(ex2_approx(x0), ex2_approx(x1));  // ex2(-inf) = 0
+      }
+      acc2[i & 3] = fadd2(acc2[i & 3], p2);
+      float p0, p1;
+      f2unpack(p2, p0, p1);
+      pk[i] = pack_bf16x2(p0, p1);
+    }
+  }
+  float a0, a1, a2, a3;
+  f2unpack(fadd2(acc2[0], acc2[1]), a0, a1);
+  f2unpack(fadd2(acc2[2], acc2[3]), a2, a3);
+  return (a0 + a1) + (a2 + a3);
+}
+
+// Position of K_j / V_j in the K/V ring's load order. With the software
+// pipeline (SEP) the order is K_0, K_1, V_0, K_2, V_1, ..., V_{n-1};
+// otherwise K_0, V_0, K_1, V_1, ...
+template <bool SEP>
+__device__ __forceinline__ int kv_pos(bool is_v, int j, int n) {
+  if (!SEP) return 2 * j + (is_v ? 1 : 0);
+  if (!is_v) return j == 0 ? 0 : 2 * j - 1;
+  return (j + 1 < n) ? 2 * j + 2 : 2 * j + 1;
 }
 
 template <int D>
@@ -82,7 +146,8 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   uint64_t* s_full = empty + NSLOT;
   uint64_t* p_full = s_full + Q_TILES;
   uint64_t* o_done = p_full + Q_TILES;
-  uint64_t* drain = o_done + Q_TILES;
+  uint64_t* s_free = o_done + Q_TILES;
+  uint64_t* drain = s_free + Q_TILES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -118,14 +183,15 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(full + i, 1);
-      mbar_init(empty + i, 1);
+      mbar_init(empty + i, Q_TILES);  // released by both MMA-issuing warps
     }
     for (int t = 0; t < Q_TILES; ++t) {
       mbar_init(s_full + t, 1);
       mbar_init(p_full + t, 128);
       mbar_init(o_done + t, 1);
+      mbar_init(s_free + t, 128);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, Q_TILES);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -141,96 +207,172 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   if (warp >= 8) {
     setmaxnreg_dec<PREFILL_PRODUCER_REGS>();
     if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      const int rq = pair * (Q_TILES * BLOCK_M);
-      mbar_arrive_expect_tx(q_full, Q_TILES * C::TILE_BYTES);
-      for (int t = 0; t < Q_TILES; ++t)
-        for (int b = 0; b < C::NBOX; ++b)
-          tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full, 64 * b, rq + t * BLOCK_M, bh);
-      int last = -1;
+      // ---------------------------------------------------------- TMA producer
+      // The whole warp runs the loop and waits; lane 0 issues the copies.
+      const bool leader = lane == 0;
+      if (leader) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        const int rq = pair * (Q_TILES * BLOCK_M);
+        mbar_arrive_expect_tx(q_full, Q_TILES * C::TILE_BYTES);
+        for (int t = 0; t < Q_TILES; ++t)
+          for (int b = 0; b < C::NBOX; ++b)
+            tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full, 64 * b, rq + t * BLOCK_M, bh);
+      }
+      int nl = 0;  // ring position of the next load
       bool ok = true;
-      for (int j = 0; ok && j < n_max; ++j) {
-        for (int w = 0; w < 2; ++w) {
-          const int n = 2 * j + w;
-          const int slot = n % NSLOT;
-          if (!mbar_wait(empty + slot, ((n / NSLOT) & 1) ^ 1, lim, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
+      auto load = [&](bool is_v, int jj) {
+        const int slot = nl % NSLOT;
+        ok = mbar_wait(empty + slot, ((nl / NSLOT) & 1) ^ 1, lim, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return;
+        if (leader) {
           mbar_arrive_expect_tx(full + slot, C::TILE_BYTES);
           for (int b = 0; b < C::NBOX; ++b)
-            tma_load_3d(sKV + slot * C::TILE_BYTES + b * C::BOX_BYTES, w ? &tmV : &tmK, full + slot, 64 * b,
-                        j * BLOCK_N, bh);
-          last = n;
+            tma_load_3d(sKV + slot * C::TILE_BYTES + b * C::BOX_BYTES, is_v ? &tmV : &tmK, full + slot, 64 * b,
+                        jj * BLOCK_N, bh);
+        }
+        ++nl;
+      };
+      // ring order matches the MMA warp's consumption order (see kv_pos)
+      if (C::SEP_P) {
+        if (n_max > 0) load(false, 0);
+        for (int jj = 0; ok && jj < n_max; ++jj) {
+          if (jj + 1 < n_max) load(false, jj + 1);
+          if (ok) load(true, jj);
+        }
+      } else {
+        for (int jj = 0; ok && jj < n_max; ++jj) {
+          load(false, jj);
+          if (ok) load(true, jj);
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // error path: let the copies already issued land before the CTA exits
         mbar_wait_drain(q_full, 0, lim);
-        for (int n = max(0, last - NSLOT + 1); n <= last; ++n)
-          mbar_wait_drain(full + (n % NSLOT), (n / NSLOT) & 1, lim);
+        for (int n = max(0, nl - NSLOT); n < nl; ++n) mbar_wait_drain(full + (n % NSLOT), (n / NSLOT) & 1, lim);
       }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+      __syncwarp();
+    } else if (warp == 9 || warp == 10) {
+      // ---------------------------------------------------------- MMA issuers
+      // One warp per Q tile (warp 9: tile 0, warp 10: tile 1). tcgen05.mma
+      // issue only runs about one instruction ahead of the tensor pipe, so
+      // every barrier wait or commit of a lone issuing warp would leave the
+      // pipe idle; with two issuers each one's waits overlap the other's MMAs.
+      // The whole warp runs the loop and waits; lane 0 issues MMAs and commits.
+      const int t = warp - 9;
+      const bool leader = lane == 0;
       bool ok = mbar_wait(q_full, 0, lim, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
-      const uint32_t sQa = smem_u32(sQ);
+      const uint32_t sQa = smem_u32(sQ) + t * C::TILE_BYTES;
       const uint32_t sKVa = smem_u32(sKV);
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int nk = 2 * j;
-        const int ks = nk % NSLOT;
-        if (!(ok = mbar_wait(full + ks, (nk / NSLOT) & 1, lim, p.status, abort_flag))) break;
-        tc_fence_after();
-        for (int t = 0; t < Q_TILES && ok; ++t) {
-          if (j >= n_t[t]) continue;
-          if (j > 0) {
-            // S_t is overwritten: the PV MMA that read P_t from it must be complete
-            if (!(ok = mbar_wait(o_done + t, (j - 1) & 1, lim, p.status, abort_flag))) break;
-            tc_fence_after();
-          }
-          const uint32_t dS = tmem + BLOCK_N * t;
+      // descriptors for ring slot 0; other slots differ only in the start-address
+      // field (bits 0-13, address >> 4)
+      uint64_t dq[D / 16], dk[D / 16], dv[BLOCK_N / 16];
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-            mma_ss(dS, sdesc_sw128(sQa + t * C::TILE_BYTES + off, 16, 1024),
-                   sdesc_sw128(sKVa + ks * C::TILE_BYTES + off, 16, 1024), C::IDESC_S, kk > 0 ? 1u : 0u);
-          }
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+        dq[kk] = sdesc_sw128(sQa + off, 16, 1024);
+        dk[kk] = sdesc_sw128(sKVa + off, 16, 1024);
+      }
+#pragma unroll
+      for (int kk = 0; kk < BLOCK_N / 16; ++kk) dv[kk] = sdesc_sw128(sKVa + kk * 2048, C::BOX_BYTES, 1024);
+      const int nt = n_t[t];
+      const uint32_t dS = tmem + BLOCK_N * t;
+      const uint32_t dO = tmem + C::O_COL + D * t;
+      const uint32_t aP = tmem + C::P_COL + C::P_STRIDE * t;
+
+      auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+        ok = mbar_wait(bar, parity, lim, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        return ok;
+      };
+      auto wait_full = [&](int pos) { return wait_bar(full + (pos % NSLOT), (pos / NSLOT) & 1); };
+      auto issue_s = [&](int pos) {  // S_t = Q_t K^T from the ring slot of `pos`
+        if (leader) {
+          const uint64_t kadd = static_cast<uint64_t>(((pos % NSLOT) * C::TILE_BYTES) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss(dS, dq[kk], dk[kk] + kadd, C::IDESC_S, kk > 0 ? 1u : 0u);
           mma_commit(s_full + t);
         }
-        if (!ok) break;
-        mma_commit(empty + ks);  // K_j slot is free once these MMAs are done
-        const int nv = 2 * j + 1;
-        const int vs = nv % NSLOT;
-        if (!(ok = mbar_wait(full + vs, (nv / NSLOT) & 1, lim, p.status, abort_flag))) break;
-        tc_fence_after();
-        for (int t = 0; t < Q_TILES && ok; ++t) {
-          if (j >= n_t[t]) continue;
-          if (!(ok = mbar_wait(p_full + t, j & 1, lim, p.status, abort_flag))) break;
-          tc_fence_after();
-          const uint32_t dO = tmem + 2 * BLOCK_N + D * t;
-          const uint32_t aP = tmem + BLOCK_N * t;
+      };
+      auto issue_pv = [&](int pos, int jj) {  // O_t (+)= P_t V from the ring slot of `pos`
+        if (leader) {
+          const uint64_t vadd = static_cast<uint64_t>(((pos % NSLOT) * C::TILE_BYTES) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-            mma_ts(dO, aP + kk * 8, sdesc_sw128(sKVa + vs * C::TILE_BYTES + kk * 2048, C::BOX_BYTES, 1024),
-                   C::IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+            mma_ts(dO, aP + kk * 8, dv[kk] + vadd, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
           mma_commit(o_done + t);
         }
-        if (!ok) break;
-        mma_commit(empty + vs);  // V_j slot is free once these MMAs are done
+      };
+      // A slot is released by both issuers (the empty barrier counts 2): by a
+      // commit when this warp's MMAs read it, by a plain arrive when they did
+      // not (a tile whose range ended or is empty). A commit from a thread with
+      // no tcgen05 operation to track is not relied on to arrive. An unused
+      // slot is first waited for (full), so the arrive lands in that load's
+      // phase: an idle warp must not run around the ring ahead of the loads.
+      auto release = [&](int pos, bool used) {
+        if (!used && !wait_full(pos)) return;
+        if (leader) {
+          if (used) mma_commit(empty + (pos % NSLOT));
+          else mbar_arrive(empty + (pos % NSLOT));
+        }
+      };
+
+      if (C::SEP_P) {
+        // Software pipeline: S_{j+1} is issued as soon as the softmax has read
+        // S_j (s_free), so the next scores are computed while it exponentiates.
+        if (ok && n_max > 0) {
+          if (nt > 0) {
+            if (wait_full(0)) issue_s(0);
+          }
+          if (ok) release(0, nt > 0);
+        }
+        for (int jj = 0; ok && jj < n_max; ++jj) {
+          if (jj + 1 < n_max) {
+            const int pk = kv_pos<true>(false, jj + 1, n_max);
+            if (jj + 1 < nt) {
+              if (!wait_full(pk) || !wait_bar(s_free + t, jj & 1)) break;
+              issue_s(pk);
+            }
+            release(pk, jj + 1 < nt);
+          }
+          const int pv = kv_pos<true>(true, jj, n_max);
+          if (jj < nt) {
+            if (!wait_full(pv) || !wait_bar(p_full + t, jj & 1)) break;
+            issue_pv(pv, jj);
+          }
+          release(pv, jj < nt);
+        }
+      } else {
+        // P aliases S in TMEM: S_{t,j} may only be written after PV_{t,j-1}
+        // (which reads P_{t,j-1} from the same columns) has completed.
+        for (int jj = 0; ok && jj < n_max; ++jj) {
+          const int pk = kv_pos<false>(false, jj, n_max);
+          if (jj < nt) {
+            if (!wait_full(pk)) break;
+            if (jj > 0 && !wait_bar(o_done + t, (jj - 1) & 1)) break;
+            issue_s(pk);
+          }
+          release(pk, jj < nt);
+          const int pv = kv_pos<false>(true, jj, n_max);
+          if (jj < nt) {
+            if (!wait_full(pv) || !wait_bar(p_full + t, jj & 1)) break;
+            issue_pv(pv, jj);
+          }
+          release(pv, jj < nt);
+        }
       }
-      // every MMA this thread issued must finish before TMEM is released
-      mma_commit(drain);
-      mbar_wait_drain(drain, 0, lim);
-    }
-    __syncwarp();
+      // every MMA both issuers issued must finish before TMEM is released
+      if (leader) {
+        if (nt > 0) mma_commit(drain);
+        else mbar_arrive(drain);
+        mbar_wait_drain(drain, 0, lim);
+      }
+      __syncwarp();
     }
   } else {
     setmaxnreg_inc<PREFILL_SOFTMAX_REGS>();
@@ -243,7 +385,8 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     const int n = n_t[t];
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + BLOCK_N * t;
-    const uint32_t tO = tmem + lane_base + 2 * BLOCK_N + D * t;
+    const uint32_t tO = tmem + lane_base + C::O_COL + D * t;
+    const uint32_t tP = tmem + lane_base + C::P_COL + C::P_STRIDE * t;
     const float sl2 = p.scale_log2;
     const int delta = p.Nk - p.Nq;
     const int diag = qi + delta;          // last key this row may see (causal)
@@ -254,9 +397,10 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       const int b = bh / p.H, h = bh % p.H;
       krow = p.keep + b * p.msb + h * p.msh + static_cast<int64_t>(qi) * p.msq;
     }
-    float m = -INFINITY;  // running max, in log2 units of the scaled score
-    float l = 0.f;        // running sum of exponentials
+    float m = -INFINITY;  // running max (possibly stale, see below), log2 units of the scaled score
+    float l = 0.f;        // running sum of exponentials on the base m
     bool ok = true;
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
 
     for (int j = 0; j < n; ++j) {
       ok = mbar_wait(s_full + t, j & 1, lim, p.status, abort_flag);
@@ -272,6 +416,10 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       reg_fence32(s + 32);
       reg_fence32(s + 64);
       reg_fence32(s + 96);
+      if (C::SEP_P) {  // S_t may be overwritten with the next tile's scores
+        tc_fence_before();
+        mbar_arrive(s_free + t);
+      }
 
       const int kbase = j * BLOCK_N;
       const bool need_mask =
@@ -294,43 +442,55 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           if (!vis) s[c] = f2u(-INFINITY);
         }
       }
-      float mx = -INFINITY;
+      // row max: 8 independent chains of three-input maxima, then a short tree
+      float mxa[8];
 #pragma unroll
-      for (int c = 0; c < BLOCK_N; ++c) mx = fmaxf(mx, u2f(s[c]));
-      const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * sl2;
-      const float m_new = fmaxf(m, m_tile);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);  // 0 while nothing was accumulated
-      const float nm = -m_use;
-      float sum = 0.f;
+      for (int a = 0; a < 8; ++a) {
+        float v = u2f(s[a * 16]);
 #pragma unroll
-      for (int ch = 0; ch < BLOCK_N / 32; ++ch) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float x0 = u2f(s[ch * 32 + 2 * i]);
-          const float x1 = u2f(s[ch * 32 + 2 * i + 1]);
-          float p0 = ex2_approx(fmaf(x0, sl2, nm));
-          float p1 = ex2_approx(fmaf(x1, sl2, nm));
-          if (need_mask) {  // masked scores are -inf; keep them at 0 even for scale 0
-            p0 = (x0 == -INFINITY) ? 0.f : p0;
-            p1 = (x1 == -INFINITY) ? 0.f : p1;
-          }
-          sum += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + ch * 16, pk);  // P (bf16 pairs) over the first 64 columns of S_t
+        for (int e = 1; e + 1 < 16; e += 2) v = fmax3(v, u2f(s[a * 16 + e]), u2f(s[a * 16 + e + 1]));
+        mxa[a] = fmaxf(v, u2f(s[a * 16 + 15]));
       }
-      l = l * alpha + sum;
-      // O_t is quiescent here: S_t,j was issued only after PV_t,j-1 completed.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      const float mx = fmaxf(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(fmax3(mxa[3], mxa[4], mxa[5]), mxa[6], mxa[7]));
+      const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+      // Lazy rescale: keep the running base m unless this tile's max exceeds it
+      // by more than RESCALE_LOG2; exponentials are then at most 2^RESCALE_LOG2,
+      // and l and O share the same (stale) base, so o / l is unchanged.
+      const bool bump = m_tile > m + C::RESCALE_LOG2;
+      const float m_new = bump ? m_tile : m;
+      const float alpha = bump ? ex2_approx(m - m_new) : 1.f;  // 0 while nothing was accumulated
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const uint64_t nm2 = f2pack(-m_use, -m_use);
+      uint32_t pk[BLOCK_N / 2];
+      const float rowsum = need_mask ? softmax_tile_p<true, C::EMU_PAIRS>(s, sl2x2, nm2, pk)
+                                     : softmax_tile_p<false, C::EMU_PAIRS>(s, sl2x2, nm2, pk);
+      if (C::SEP_P && j > 0) {
+        // P_t and O_t are free once PV_{t,j-1} has completed; it ran while
+        // the exponentials above were computed
+        ok = mbar_wait(o_done + t, (j - 1) & 1, lim, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st32(tP, pk);
+      tmem_st32(tP + 32, pk + 32);
+      l = fmaf(l, alpha, rowsum);
+      // O_t is quiescent here: PV_{t,j-1} has completed (waited above, or before
+      // S_{t,j} was issued) and PV_{t,j} waits for p_full.
+      if (j > 0 && __any_sync(0xffffffffu, bump)) {
+        const uint64_t al2 = f2pack(alpha, alpha);
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
           tmem_ld32(tO + ch * 32, o);
           tmem_ld_wait32(o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+          for (int i = 0; i < 16; ++i) {
+            float y0, y1;
+            f2unpack(fmul2(f2pack(u2f(o[2 * i]), u2f(o[2 * i + 1])), al2), y0, y1);
+            o[2 * i] = f2u(y0);
+            o[2 * i + 1] = f2u(y1);
+          }
           tmem_st32(tO + ch * 32, o);
         }
       }

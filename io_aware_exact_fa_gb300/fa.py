@@ -43,6 +43,7 @@ EXPORTS = {
     "fa_set_wait_limit_ns": (None, [_u64]),
     "fa_get_wait_limit_ns": (_u64, []),
     "fa_selftest_wait_timeout": (_i, [_u64, _vp]),
+    "fa_selftest_exp2": (_i, [_vp, _vp, _i, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_last_error_detail": (ctypes.c_char_p, []),
     "fa_launch_count": (_u64, []),
@@ -162,6 +163,14 @@ def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
 
 def selftest_wait_timeout(limit_ns: int, stream: Optional[torch.cuda.Stream] = None) -> int:
     return int(_lib.fa_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream)))
+
+
+def selftest_exp2(x: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """2^x through the device FMA-pipe exponential used inside the prefill softmax."""
+    _need(x, "x", torch.float32)
+    y = torch.empty_like(x)
+    _check(_lib.fa_selftest_exp2(x.data_ptr(), y.data_ptr(), x.numel(), _stream_ptr(stream)), "fa_selftest_exp2")
+    return y
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -93,6 +93,7 @@ def test_host_validation_before_launch(lib):
     assert f(P + 8, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, None) == 2         # misaligned q
     assert b"aligned" in lib.fa_last_error_detail()
     assert f(P, P, P, P, None, 1, 1, 0, 8, 64, 0.125, 0, None) == 0             # Nq = 0: no-op
+    assert f(None, None, None, None, None, 1, 1, 0, 8, 64, 0.125, 0, None) == 0  # ... even with NULLs
     assert f(P, P, P, P, None, 1 << 16, 1 << 16, 8, 8, 64, 0.125, 0, None) == 1  # B*H too large
 
 

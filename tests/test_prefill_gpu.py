@@ -217,3 +217,16 @@ def test_prefill_32k_d128_causal_keypad(fa):
     w = W.WORKLOADS["prefill_32k_pad"]
     keep = W.key_padding_keep(w.B, w.H, w.Nk, w.pad_heads, w.pad_from)
     print(_sampled(fa, w, True, keep=keep, full_heads=0, rows_per_head=96))
+
+
+def test_fma_pipe_exp2_error_bound(fa):
+    """The FMA-pipe exponential stays within its stated 7.5e-5 relative error of 2^x."""
+    x = torch.cat([torch.linspace(-125.0, 127.0, 1_000_001), torch.tensor([0.0, -0.5, 0.5, 8.0, -20.25])])
+    y = fa.selftest_exp2(x.cuda()).cpu().double()
+    ref = torch.exp2(x.double())
+    rel = ((y - ref).abs() / ref).max().item()
+    assert rel < 8e-5, rel
+    # below the clamp (x < -125) the result stays at about 2^-125, negligible next
+    # to the row maximum's 2^0
+    y2 = fa.selftest_exp2(torch.tensor([-126.0, -200.0, -1000.0], device="cuda")).cpu().double()
+    assert torch.all(y2 <= 2.0 ** -124) and torch.all(y2 > 0)
