@@ -108,6 +108,33 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
                             int B, int H, int Nk, int d, float scale, int num_splits,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of the static device scratch behind fa_decode_splitkv_noalloc. */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES (20u << 20)
+
+/* Split-KV decode for callers that cannot allocate device memory. (The pages
+ * have no counterpart: this is an interface variant, not part of the method.)
+ * Some callers only hold the input and output buffers: a plugin or kernel
+ * interface that passes no workspace, or a serving loop that must not call
+ * cudaMalloc/cudaFree because those calls can synchronise the device or
+ * because another allocator owns the device memory. This entry point takes
+ * the same arguments as fa_decode_splitkv without the workspace, allocates
+ * nothing, and keeps the per-split partial states in one static device array
+ * of FA_DECODE_NOALLOC_SCRATCH_BYTES that every GPU loading the library
+ * holds until the process exits. It computes exactly what fa_decode_splitkv
+ * computes, with the same kernels.
+ *   - Requests needing more scratch than that (fa_decode_workspace_size() >
+ *     FA_DECODE_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE and launch
+ *     nothing; use fa_decode_splitkv with a caller workspace instead.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (different streams, or host threads without ordering) race and corrupt
+ *     each other's results. Calls ordered on one stream are safe; the array
+ *     needs no clearing between them because every partial is rewritten. */
+fa_status fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                    int B, int H, int Nk, int d, float scale, int num_splits, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_ERR_TIMEOUT if a bounded wait gave up since the
  * last call, FA_ERR_CUDA if the stream reported an error, else FA_OK. */

@@ -17,6 +17,10 @@
 // Merge kernel: one CTA per (b, h), one thread per output element.
 #include <cuda_bf16.h>
 
+#include <cstdio>
+#include <mutex>
+
+#include "fa.h"
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -244,3 +248,65 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int* status, cudaSt
 }
 
 }  // namespace fa
+
+// ---------------------------------------------------------------------------
+// Split-KV decode without any allocation by the caller or the library.
+//
+// Some callers of this library cannot allocate device memory: a plugin or
+// kernel interface that hands over only the input and output buffers, a
+// serving loop that must not call cudaMalloc/cudaFree (they can synchronise
+// the device) or whose device memory is entirely owned by another allocator.
+// For them the decode scratch (the per-split partial (o, m, l) states) lives
+// in one file-scope device array, allocated once when the library's device
+// code is loaded and held by every GPU that loads it until the process exits.
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[FA_DECODE_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+
+// Per-device set-up, done by the first call on each device (with that device
+// current): the array's name is only a host-side stand-in, so its device
+// address is looked up and cached.
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" fa_status fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                               float* lse, int B, int H, int Nk, int d, float scale,
+                                               int num_splits, void* stream) {
+  const size_t need = fa_decode_workspace_size(B, H, d, num_splits);
+  if (need == 0)  // invalid sizes: let the regular entry point report them
+    return fa_decode_splitkv(q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, num_splits, nullptr, 0, stream);
+  if (need > FA_DECODE_NOALLOC_SCRATCH_BYTES) {
+    fa_set_error_detail("decode needs %zu bytes of scratch; the static scratch holds %zu (use fa_decode_splitkv "
+                        "with a caller-provided workspace)",
+                        need, static_cast<size_t>(FA_DECODE_NOALLOC_SCRATCH_BYTES));
+    return FA_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  const cudaError_t e = scratch_address(&scratch);
+  if (e != cudaSuccess) {
+    fa_set_error_detail("cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
+    return FA_ERR_CUDA;
+  }
+  // every partial is written by the split kernel before the merge reads it,
+  // so the shared scratch needs no clearing between calls
+  return fa_decode_splitkv(q, k_cache, v_cache, o, lse, B, H, Nk, d, scale, num_splits, scratch,
+                           FA_DECODE_NOALLOC_SCRATCH_BYTES, stream);
+}

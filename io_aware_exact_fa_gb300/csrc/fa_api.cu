@@ -116,6 +116,14 @@ fa_status check_scale(float scale) {
 
 }  // namespace
 
+// Set the calling thread's error detail (used by entry points in other files).
+void fa_set_error_detail(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_detail, sizeof(t_detail), fmt, ap);
+  va_end(ap);
+}
+
 extern "C" {
 
 const char* fa_status_string(fa_status s) {

@@ -5,6 +5,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+// Set the calling thread's error detail string (fa_last_error_detail).
+void fa_set_error_detail(const char* fmt, ...);
+
 namespace fa {
 
 // Bits of the device status word (one word per device, cleared by

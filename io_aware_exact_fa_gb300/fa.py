@@ -39,6 +39,7 @@ EXPORTS = {
     "fa_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i64, _i64, _i64, _vp]),
     "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_decode_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
+    "fa_decode_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_get_device_status": (_i, [_vp]),
     "fa_set_wait_limit_ns": (None, [_u64]),
     "fa_get_wait_limit_ns": (_u64, []),
@@ -153,6 +154,31 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, scale:
                                 int(num_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                 _stream_ptr(stream))
     _check(rc, "fa_decode_splitkv")
+    return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 20 << 20
+
+
+def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, scale: Optional[float] = None,
+                   num_splits: int = 16, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   with_lse: bool = True, stream: Optional[torch.cuda.Stream] = None):
+    """Split-KV decode using the library's static scratch (no workspace); see fa.h."""
+    _need(q, "q"); _need(k_cache, "k_cache"); _need(v_cache, "v_cache")
+    B, H, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes one query token per (b, h): q must be [B, H, 1, d]")
+    Nk = k_cache.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if with_lse and lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    rc = _lib.fa_decode_splitkv_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                        lse.data_ptr() if lse is not None else None, B, H, Nk, d, float(scale),
+                                        int(num_splits), _stream_ptr(stream))
+    _check(rc, "fa_decode_splitkv_noalloc")
     return out, lse
 
 
