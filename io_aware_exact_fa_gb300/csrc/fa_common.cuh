@@ -19,10 +19,13 @@ constexpr unsigned int FA_DEV_TIMEOUT = 1u;   // a bounded wait ran out
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_N = 128;
 constexpr int Q_TILES = 2;
-constexpr int PREFILL_THREADS = 384;   // 2 softmax warpgroups + 1 producer warpgroup (TMA, MMA, 2 idle)
+constexpr int PREFILL_THREADS = 384;       // 2 softmax warpgroups + 1 producer warpgroup
+constexpr int PREFILL_SOFTMAX_WARPS = 8;   // warps 0-3: Q tile 0, warps 4-7: Q tile 1
+constexpr int PREFILL_TMA_WARP = 8;
+constexpr int PREFILL_MMA_WARP0 = 9;       // warps 9, 10 issue MMAs (one per Q tile); 11 idle
 // Register split after set-up (setmaxnreg): the launch gives every thread
-// PREFILL_LAUNCH_REGS; per SM sub-partition one warp of each warpgroup, so
-// 2 * SOFTMAX + PRODUCER must not exceed 3 * PREFILL_LAUNCH_REGS.
+// PREFILL_LAUNCH_REGS; each SM sub-partition holds one warp of every
+// warpgroup, so 2 * SOFTMAX + PRODUCER must not exceed 3 * PREFILL_LAUNCH_REGS.
 constexpr int PREFILL_LAUNCH_REGS = 168;
 constexpr int PREFILL_SOFTMAX_REGS = 224;
 constexpr int PREFILL_PRODUCER_REGS = 56;

@@ -272,12 +272,9 @@ __device__ __forceinline__ uint64_t exp2_fma2(uint64_t x) {
   float x0, x1;
   f2unpack(x, x0, x1);
   x = f2pack(fmaxf(x0, -125.0f), fmaxf(x1, -125.0f));
-  const uint64_t sh = f2pack(kShift, kShift);
-  const uint64_t t = fadd2(x, sh);                    // j in the low bits
+  const uint64_t t = fadd2(x, f2pack(kShift, kShift));       // j = round(x) sits in the low bits of t
   const uint64_t j = fadd2(t, f2pack(-kShift, -kShift));
-  float j0, j1;
-  f2unpack(j, j0, j1);
-  const uint64_t f = fadd2(x, f2pack(-j0, -j1));      // f = x - j in [-1/2, 1/2]
+  const uint64_t f = ffma2(j, f2pack(-1.0f, -1.0f), x);       // f = x - j in [-1/2, 1/2]
   uint64_t p = ffma2(f2pack(0.05517132207751274f, 0.05517132207751274f), f,
                      f2pack(0.2426113337278366f, 0.2426113337278366f));
   p = ffma2(p, f, f2pack(0.6932610869407654f, 0.6932610869407654f));
@@ -285,8 +282,9 @@ __device__ __forceinline__ uint64_t exp2_fma2(uint64_t x) {
   float p0, p1, t0, t1;
   f2unpack(p, p0, p1);
   f2unpack(t, t0, t1);
-  const float r0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
-  const float r1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
+  // 2^f * 2^j: add j to the exponent field
+  const float r0 = __uint_as_float((__float_as_uint(t0) << 23) + __float_as_uint(p0));
+  const float r1 = __uint_as_float((__float_as_uint(t1) << 23) + __float_as_uint(p1));
   return f2pack(r0, r1);
 }
 

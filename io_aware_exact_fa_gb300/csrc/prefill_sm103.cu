@@ -34,16 +34,32 @@
 
 namespace fa {
 
+// Tuning knobs (compile time): exponential pairs per 16 computed on the FMA
+// pipe, and whether the second Q tile starts half a period late.
+#ifndef FA_EMU_PAIRS_D64
+#define FA_EMU_PAIRS_D64 0
+#endif
+#ifndef FA_EMU_PAIRS_D128
+#define FA_EMU_PAIRS_D128 0
+#endif
+#ifndef FA_STAGGER
+#define FA_STAGGER 1
+#endif
+#ifndef FA_STAGGER_MIN_TILES
+#define FA_STAGGER_MIN_TILES 8   // only units this long amortise the delayed start
+#endif
+
 template <int D>
 struct PrefillCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int TILE_BYTES = BLOCK_N * D * 2;  // one Q, K or V tile (128 rows x D bf16)
   static constexpr int BOX_BYTES = 128 * 128;         // one TMA box: 128 rows x 64 bf16
   static constexpr int NBOX = D / 64;
-  static constexpr int NSLOT = (D == 128) ? 4 : 8;    // K/V ring slots (K and V alternate)
+  static constexpr int NSLOT = (D == 128) ? 2 : 4;    // ring slots, each holding one K tile and one V tile
+  static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = Q_TILES * TILE_BYTES;
-  static constexpr int BAR_OFF = KV_OFF + NSLOT * TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSLOT * SLOT_BYTES;
   // TMEM columns: S_0 [0,128), S_1 [128,256), O_t at O_COL + D*t; with
   // SEP_P (d = 64) P_t gets its own 64 columns at P_COL + 64*t, otherwise P_t
   // overwrites the first 64 columns of S_t.
@@ -60,7 +76,7 @@ struct PrefillCfg {
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);     // V is MN-major
   // Softmax tuning: exponential pairs (of 16 per 32 columns) computed on the
   // FMA pipe instead of the MUFU unit, and the lazy-rescale threshold.
-  static constexpr int EMU_PAIRS = 0;
+  static constexpr int EMU_PAIRS = (D == 64) ? FA_EMU_PAIRS_D64 : FA_EMU_PAIRS_D128;
   static constexpr float RESCALE_LOG2 = 8.0f;
 };
 
@@ -79,9 +95,8 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 
 // One query row's scores s[0..127] (fp32 bit patterns, masked ones -inf) ->
 // P = 2^(s * sl2 - m) as 64 bf16 pairs in pk_all, returning the row sum of
-// the fp32 exponentials. EMU pairs of every 16
-// use the FMA-pipe exponential. With MASKED, -inf scores give exactly 0 on
-// both exponential paths.
+// the fp32 exponentials. EMU pairs of every 16 use the FMA-pipe exponential.
+// With MASKED, -inf scores give exactly 0 on both exponential paths.
 template <bool MASKED, int EMU>
 __device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x2, uint64_t nm2, uint32_t* pk_all) {
   uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
@@ -119,14 +134,16 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x
   return (a0 + a1) + (a2 + a3);
 }
 
-// Position of K_j / V_j in the K/V ring's load order. With the software
-// pipeline (SEP) the order is K_0, K_1, V_0, K_2, V_1, ..., V_{n-1};
-// otherwise K_0, V_0, K_1, V_1, ...
-template <bool SEP>
-__device__ __forceinline__ int kv_pos(bool is_v, int j, int n) {
-  if (!SEP) return 2 * j + (is_v ? 1 : 0);
-  if (!is_v) return j == 0 ? 0 : 2 * j - 1;
-  return (j + 1 < n) ? 2 * j + 2 : 2 * j + 1;
+// Waits on two barriers. Both first polls are issued back to back, so when
+// both phases have already completed the thread pays one barrier round trip
+// instead of two.
+__device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t lim,
+                                           unsigned int* status, volatile int* abort) {
+  const bool ra = mbar_try_wait(smem_u32(a), pa);
+  const bool rb = mbar_try_wait(smem_u32(b), pb);
+  if (!ra && !mbar_wait(a, pa, lim, status, abort)) return false;
+  if (!rb && !mbar_wait(b, pb, lim, status, abort)) return false;
+  return true;
 }
 
 template <int D>
@@ -195,7 +212,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == PREFILL_MMA_WARP0) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -204,9 +221,9 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 8) {
+  if (warp >= PREFILL_SOFTMAX_WARPS) {
     setmaxnreg_dec<PREFILL_PRODUCER_REGS>();
-    if (warp == 8) {
+    if (warp == PREFILL_TMA_WARP) {
       // ---------------------------------------------------------- TMA producer
       // The whole warp runs the loop and waits; lane 0 issues the copies.
       const bool leader = lane == 0;
@@ -220,33 +237,22 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           for (int b = 0; b < C::NBOX; ++b)
             tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full, 64 * b, rq + t * BLOCK_M, bh);
       }
-      int nl = 0;  // ring position of the next load
+      int nl = 0;  // number of K/V tiles loaded so far (ring position)
       bool ok = true;
-      auto load = [&](bool is_v, int jj) {
-        const int slot = nl % NSLOT;
-        ok = mbar_wait(empty + slot, ((nl / NSLOT) & 1) ^ 1, lim, p.status, abort_flag);
+      for (int jj = 0; ok && jj < n_max; ++jj) {
+        const int slot = jj % NSLOT;
+        ok = mbar_wait(empty + slot, ((jj / NSLOT) & 1) ^ 1, lim, p.status, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
-        if (!ok) return;
+        if (!ok) break;
         if (leader) {
-          mbar_arrive_expect_tx(full + slot, C::TILE_BYTES);
+          uint8_t* dst = sKV + slot * C::SLOT_BYTES;
+          mbar_arrive_expect_tx(full + slot, C::SLOT_BYTES);
           for (int b = 0; b < C::NBOX; ++b)
-            tma_load_3d(sKV + slot * C::TILE_BYTES + b * C::BOX_BYTES, is_v ? &tmV : &tmK, full + slot, 64 * b,
-                        jj * BLOCK_N, bh);
+            tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full + slot, 64 * b, jj * BLOCK_N, bh);
+          for (int b = 0; b < C::NBOX; ++b)
+            tma_load_3d(dst + C::TILE_BYTES + b * C::BOX_BYTES, &tmV, full + slot, 64 * b, jj * BLOCK_N, bh);
         }
         ++nl;
-      };
-      // ring order matches the MMA warp's consumption order (see kv_pos)
-      if (C::SEP_P) {
-        if (n_max > 0) load(false, 0);
-        for (int jj = 0; ok && jj < n_max; ++jj) {
-          if (jj + 1 < n_max) load(false, jj + 1);
-          if (ok) load(true, jj);
-        }
-      } else {
-        for (int jj = 0; ok && jj < n_max; ++jj) {
-          load(false, jj);
-          if (ok) load(true, jj);
-        }
       }
       if (!ok && leader) {
         // error path: let the copies already issued land before the CTA exits
@@ -254,14 +260,14 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         for (int n = max(0, nl - NSLOT); n < nl; ++n) mbar_wait_drain(full + (n % NSLOT), (n / NSLOT) & 1, lim);
       }
       __syncwarp();
-    } else if (warp == 9 || warp == 10) {
+    } else if (warp == PREFILL_MMA_WARP0 || warp == PREFILL_MMA_WARP0 + 1) {
       // ---------------------------------------------------------- MMA issuers
-      // One warp per Q tile (warp 9: tile 0, warp 10: tile 1). tcgen05.mma
+      // One warp per Q tile (tile 0 first). tcgen05.mma
       // issue only runs about one instruction ahead of the tensor pipe, so
       // every barrier wait or commit of a lone issuing warp would leave the
       // pipe idle; with two issuers each one's waits overlap the other's MMAs.
       // The whole warp runs the loop and waits; lane 0 issues MMAs and commits.
-      const int t = warp - 9;
+      const int t = warp - PREFILL_MMA_WARP0;
       const bool leader = lane == 0;
       bool ok = mbar_wait(q_full, 0, lim, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
@@ -290,18 +296,25 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         tc_fence_after();
         return ok;
       };
-      auto wait_full = [&](int pos) { return wait_bar(full + (pos % NSLOT), (pos / NSLOT) & 1); };
-      auto issue_s = [&](int pos) {  // S_t = Q_t K^T from the ring slot of `pos`
+      auto wait_bar2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb) {
+        ok = mbar_wait2(a, pa, b, pb, lim, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        return ok;
+      };
+      auto full_bar = [&](int jj) { return full + (jj % NSLOT); };
+      auto full_par = [&](int jj) { return static_cast<uint32_t>((jj / NSLOT) & 1); };
+      auto issue_s = [&](int jj) {  // S_t = Q_t K_jj^T
         if (leader) {
-          const uint64_t kadd = static_cast<uint64_t>(((pos % NSLOT) * C::TILE_BYTES) >> 4);
+          const uint64_t kadd = static_cast<uint64_t>(((jj % NSLOT) * C::SLOT_BYTES) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) mma_ss(dS, dq[kk], dk[kk] + kadd, C::IDESC_S, kk > 0 ? 1u : 0u);
           mma_commit(s_full + t);
         }
       };
-      auto issue_pv = [&](int pos, int jj) {  // O_t (+)= P_t V from the ring slot of `pos`
+      auto issue_pv = [&](int jj) {  // O_t (+)= P_t V_jj
         if (leader) {
-          const uint64_t vadd = static_cast<uint64_t>(((pos % NSLOT) * C::TILE_BYTES) >> 4);
+          const uint64_t vadd = static_cast<uint64_t>(((jj % NSLOT) * C::SLOT_BYTES + C::TILE_BYTES) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BLOCK_N / 16; ++kk)
             mma_ts(dO, aP + kk * 8, dv[kk] + vadd, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
@@ -314,56 +327,47 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       // no tcgen05 operation to track is not relied on to arrive. An unused
       // slot is first waited for (full), so the arrive lands in that load's
       // phase: an idle warp must not run around the ring ahead of the loads.
-      auto release = [&](int pos, bool used) {
-        if (!used && !wait_full(pos)) return;
+      auto release = [&](int jj, bool used) {
+        if (!used && !wait_bar(full_bar(jj), full_par(jj))) return;
         if (leader) {
-          if (used) mma_commit(empty + (pos % NSLOT));
-          else mbar_arrive(empty + (pos % NSLOT));
+          if (used) mma_commit(empty + (jj % NSLOT));
+          else mbar_arrive(empty + (jj % NSLOT));
         }
       };
+
+      // Ping-pong: the second Q tile starts once the first tile's first
+      // softmax is done, so one tile's exponentials overlap the other tile's
+      // MMAs instead of both tiles competing for the same unit at once.
+      if (FA_STAGGER && t == 1 && n_t[0] >= FA_STAGGER_MIN_TILES && nt > 0) wait_bar(p_full + 0, 0);
 
       if (C::SEP_P) {
         // Software pipeline: S_{j+1} is issued as soon as the softmax has read
         // S_j (s_free), so the next scores are computed while it exponentiates.
-        if (ok && n_max > 0) {
-          if (nt > 0) {
-            if (wait_full(0)) issue_s(0);
-          }
-          if (ok) release(0, nt > 0);
-        }
+        if (ok && nt > 0 && wait_bar(full_bar(0), full_par(0))) issue_s(0);
         for (int jj = 0; ok && jj < n_max; ++jj) {
-          if (jj + 1 < n_max) {
-            const int pk = kv_pos<true>(false, jj + 1, n_max);
-            if (jj + 1 < nt) {
-              if (!wait_full(pk) || !wait_bar(s_free + t, jj & 1)) break;
-              issue_s(pk);
-            }
-            release(pk, jj + 1 < nt);
+          if (jj + 1 < nt) {
+            if (!wait_bar2(full_bar(jj + 1), full_par(jj + 1), s_free + t, jj & 1)) break;
+            issue_s(jj + 1);
           }
-          const int pv = kv_pos<true>(true, jj, n_max);
           if (jj < nt) {
-            if (!wait_full(pv) || !wait_bar(p_full + t, jj & 1)) break;
-            issue_pv(pv, jj);
+            if (!wait_bar(p_full + t, jj & 1)) break;
+            issue_pv(jj);
           }
-          release(pv, jj < nt);
+          release(jj, jj < nt);
         }
       } else {
         // P aliases S in TMEM: S_{t,j} may only be written after PV_{t,j-1}
         // (which reads P_{t,j-1} from the same columns) has completed.
         for (int jj = 0; ok && jj < n_max; ++jj) {
-          const int pk = kv_pos<false>(false, jj, n_max);
           if (jj < nt) {
-            if (!wait_full(pk)) break;
-            if (jj > 0 && !wait_bar(o_done + t, (jj - 1) & 1)) break;
-            issue_s(pk);
+            const bool w = (jj > 0) ? wait_bar2(full_bar(jj), full_par(jj), o_done + t, (jj - 1) & 1)
+                                    : wait_bar(full_bar(jj), full_par(jj));
+            if (!w) break;
+            issue_s(jj);
+            if (!wait_bar(p_full + t, jj & 1)) break;
+            issue_pv(jj);
           }
-          release(pk, jj < nt);
-          const int pv = kv_pos<false>(true, jj, n_max);
-          if (jj < nt) {
-            if (!wait_full(pv) || !wait_bar(p_full + t, jj & 1)) break;
-            issue_pv(pv, jj);
-          }
-          release(pv, jj < nt);
+          release(jj, jj < nt);
         }
       }
       // every MMA both issuers issued must finish before TMEM is released
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == PREFILL_MMA_WARP0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
