@@ -11,7 +11,9 @@ Every timed launch is bracketed by CUDA events on the launching stream; the
 L2 (129 MB) is flushed between steps by writing a 256 MB buffer outside the
 events (the prefill inputs, 67 MB, would otherwise stay L2-resident).
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--prefill-workload NAME]
+(the default prefill workload is the headline one; the others time the d=128
+8k / 32k causal workloads through the same harness)
 Under torchrun each rank runs the same per-GPU workload (weak scaling, no
 data-path collective); rank 0 prints one JSON line.
 """
@@ -209,6 +211,9 @@ def main():
                     help="run one part of the step only (small profiling runs)")
     ap.add_argument("--decode-b", type=int, default=0, help="override the decode batch (profiling a small case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--prefill-workload", default=PREFILL,
+                    choices=["prefill_2k", "prefill_8k", "prefill_32k", "prefill_32k_pad"],
+                    help="prefill workload of the step (default: the 2k / d=64 headline workload)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -230,7 +235,8 @@ def main():
 
     do_p = args.only in ("all", "prefill")
     do_d = args.only in ("all", "decode")
-    wp = W.WORKLOADS[PREFILL]
+    wp = W.WORKLOADS[args.prefill_workload]
+    modes = list(wp.causal_modes)
     wd = W.WORKLOADS[DECODE]
     if args.decode_b:
         import dataclasses
@@ -239,6 +245,10 @@ def main():
         q, k, v = W.make_qkv(wp.B, wp.H, wp.Nq, wp.Nk, wp.d, seed=rank, device="cuda")
         o = torch.empty_like(q)
         lse = torch.empty(wp.B, wp.H, wp.Nq, dtype=torch.float32, device=dev)
+        keep_words, mstrides = None, (0, 0, 0)
+        if wp.pad_heads:
+            words = W.pack_keep_bits(W.key_padding_keep(wp.B, wp.H, wp.Nk, wp.pad_heads, wp.pad_from))
+            keep_words, mstrides = words.to(dev), W.mask_strides(words)
     if do_d:
         dq, dk, dv = W.make_qkv(wd.B, wd.H, 1, wd.Nk, wd.d, seed=1000 + rank, device="cuda")
         do = torch.empty_like(dq)
@@ -249,29 +259,28 @@ def main():
     stream = torch.cuda.current_stream()
 
     def prefill(causal):
-        fa.fwd(q, k, v, scale=wp.scale, causal=causal, out=o, lse=lse)
+        fa.fwd(q, k, v, scale=wp.scale, causal=causal, keep_bits=keep_words, mask_strides=mstrides, out=o, lse=lse)
 
     def decode():
         fa.decode(dq, dk, dv, scale=wd.scale, num_splits=wd.num_splits, workspace=ws, out=do, lse=dlse)
 
     def step_body(e):
+        # events: e[0] .. e[len(modes)] bracket the prefill launches, then decode
         e[0].record(stream)
-        if do_p:
-            prefill(False)
-        e[1].record(stream)
-        if do_p:
-            prefill(True)
-        e[2].record(stream)
+        for i, causal in enumerate(modes):
+            if do_p:
+                prefill(causal)
+            e[i + 1].record(stream)
         if do_d:
             decode()
-        e[3].record(stream)
+        e[len(modes) + 1].record(stream)
 
     warm = max(3, args.warmup)
     for _ in range(warm):
         flush.zero_()
         if do_p:
-            prefill(False)
-            prefill(True)
+            for causal in modes:
+                prefill(causal)
         if do_d:
             decode()
     torch.cuda.synchronize()
@@ -279,7 +288,7 @@ def main():
         raise RuntimeError("device status not OK after warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(modes) + 2)] for _ in range(K)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.2)
@@ -301,14 +310,16 @@ def main():
     if fa.device_status() != fa.FA_OK:
         raise RuntimeError("device status not OK after the timed region")
 
-    t_nc = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
-    t_c = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
-    t_d = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
-    times = torch.tensor([t_nc, t_c, t_d], dtype=torch.float64, device=dev)
+    nm = len(modes)
+    t_modes = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / 1e3 for i in range(nm)]
+    t_d = sum(e[nm].elapsed_time(e[nm + 1]) for e in ev) / 1e3
+    times = torch.tensor(t_modes + [t_d], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    t_nc, t_c, t_d = times.tolist()
-    f_nc, f_c = wp.flops(False), wp.flops(True)
+    times = times.tolist()
+    t_modes, t_d = times[:nm], times[nm]
+    f_modes = [wp.flops(c) for c in modes]
+    t_p, f_p = sum(t_modes), sum(f_modes)
     peaks = measured_peaks()
     dec_bytes = wd.io_bytes()
 
@@ -319,8 +330,8 @@ def main():
         ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_e)]
         if do_p:
             hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
-            ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
-            hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
+            ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in modes]
+            hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in modes]
         if do_d:
             hdq = dq.cpu().pin_memory()
             hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
@@ -333,7 +344,7 @@ def main():
                 q.copy_(hq, non_blocking=True)
                 k.copy_(hk, non_blocking=True)
                 v.copy_(hv, non_blocking=True)
-                for c, causal in enumerate((False, True)):
+                for c, causal in enumerate(modes):
                     prefill(causal)
                     ho[c].copy_(o, non_blocking=True)
                     hl[c].copy_(lse, non_blocking=True)
@@ -348,8 +359,9 @@ def main():
         te_p = sum(e[0].elapsed_time(e[1]) for e in ee) / 1e3
         te_d = sum(e[1].elapsed_time(e[2]) for e in ee) / 1e3
         if do_p:
-            e2e = {"value": world * n_e * (f_nc + f_c) / te_p / 1e12, "unit": "TFLOP/s",
-                   "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": 2 * (o.numel() * 2 + lse.numel() * 4)}
+            e2e = {"value": world * n_e * f_p / te_p / 1e12, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": 3 * q.numel() * 2,
+                   "d2h_bytes_per_step": nm * (o.numel() * 2 + lse.numel() * 4)}
         if do_d:
             dec_e2e = {"value": world * n_e * dec_bytes / te_d / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": dq.numel() * 2, "d2h_bytes_per_step": do.numel() * 2 + dlse.numel() * 4,
@@ -357,7 +369,7 @@ def main():
 
     # ---- CPU baseline: the oracle on the host cores, a bounded sample
     cpu = None
-    if rank == 0 and world == 1 and args.cpu_budget > 0 and do_p:
+    if rank == 0 and world == 1 and args.cpu_budget > 0 and do_p and args.prefill_workload == PREFILL:
         f, s, heads = oracle_prefill_sample(wp, args.cpu_budget)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{heads} whole heads (1 head = {wp.Nq}x{wp.Nk}, d={wp.d}) of {wp.name}, "
@@ -369,21 +381,23 @@ def main():
         return 0
     line = {
         "metric": METRIC,
-        "value": world * K * (f_nc + f_c) / (t_nc + t_c) / 1e12 if do_p else None,
+        "value": world * K * f_p / t_p / 1e12 if do_p else None,
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": K,
         "warmup": warm,
-        "ms_per_step": (t_nc + t_c + t_d) / K * 1e3,
+        "ms_per_step": (t_p + t_d) / K * 1e3,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": (f"{wp.name} (non-causal + causal)" if do_p else "")
+        "config": {"workload": (f"{wp.name} ({' + '.join('causal' if c else 'non-causal' for c in modes)})"
+                                if do_p else "")
                    + (" + " if do_p and do_d else "") + (wd.name if do_d else ""),
                    "B": wp.B, "H": wp.H, "Nq": wp.Nq, "Nk": wp.Nk, "d": wp.d, "scale": wp.scale,
-                   "causal": [False, True],
+                   "causal": modes,
+                   "key_padding": ({"heads_below": wp.pad_heads, "keys_from": wp.pad_from} if wp.pad_heads else None),
                    "decode": {"B": wd.B, "H": wd.H, "Nk": wd.Nk, "d": wd.d, "num_splits": wd.num_splits},
                    "l2": "flushed between steps (256 MB write outside the timed events)",
                    "parallelism": f"replicas x{world}"},
@@ -394,13 +408,16 @@ def main():
         "wall_s_timed": t_wall1 - t_wall0,
     }
     if do_p:
-        ach = K * (f_nc + f_c) / (t_nc + t_c) / 1e12
+        ach = K * f_p / t_p / 1e12
         line["roofline"] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": ach / peaks["bf16_tflops"],
                             "traffic": recorded_traffic("prefill_sm103.cu", wp.name),
-                            "kernel": "fa_prefill_kernel<64>", "peak_source": f"{peaks['source']} bf16 burst",
-                            "ms_noncausal": t_nc / K * 1e3, "ms_causal": t_c / K * 1e3,
-                            "tflops_noncausal": K * f_nc / t_nc / 1e12, "tflops_causal": K * f_c / t_c / 1e12}
+                            "kernel": f"fa_prefill_kernel<{wp.d}>", "peak_source": f"{peaks['source']} bf16 burst",
+                            "flop_convention": "4*B*H*Nq*Nk*d per non-causal launch, halved for causal"}
+        for c, tm, fm in zip(modes, t_modes, f_modes):
+            tag = "causal" if c else "noncausal"
+            line["roofline"][f"ms_{tag}"] = tm / K * 1e3
+            line["roofline"][f"tflops_{tag}"] = K * fm / tm / 1e12
     if do_d:
         ach = K * dec_bytes / t_d / 1e9
         line["decode"] = {"value": world * ach, "unit": "GB/s", "ms": t_d / K * 1e3, "bytes": dec_bytes,
