@@ -194,7 +194,20 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     }
     n_t[t] = n;
   }
-  const int n_max = max(n_t[0], n_t[1]);
+  int* kv_keep_slot = reinterpret_cast<int*>(smem + C::MISC_OFF + 8);
+  if (p.keep != nullptr && p.msq == 0 && warp == PREFILL_SOFTMAX_WARPS + 3) {
+    // One key mask for every row of this head: tiles after the last one with
+    // any key kept are skipped by every role.
+    const int b = bh / p.H, h = bh % p.H;
+    const uint32_t* kb = p.keep + b * p.msb + h * p.msh;
+    const int nwords = (p.Nk + 31) >> 5;
+    int last = -1;
+    for (int wi = lane; wi < nwords; wi += 32)
+      if (__ldg(kb + wi) != 0u) last = wi;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, off));
+    if (lane == 0) *kv_keep_slot = (last < 0) ? 0 : (last * 32) / BLOCK_N + 1;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -220,6 +233,12 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (p.keep != nullptr && p.msq == 0) {
+    const int kv_keep = *kv_keep_slot;
+#pragma unroll
+    for (int t = 0; t < Q_TILES; ++t) n_t[t] = min(n_t[t], kv_keep);
+  }
+  const int n_max = max(n_t[0], n_t[1]);
 
   if (warp >= PREFILL_SOFTMAX_WARPS) {
     setmaxnreg_dec<PREFILL_PRODUCER_REGS>();
@@ -426,17 +445,21 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       }
 
       const int kbase = j * BLOCK_N;
-      const bool need_mask =
-          (kbase + BLOCK_N > p.Nk) || (p.causal && kbase + BLOCK_N - 1 > tile_lim) || (p.keep != nullptr);
-      if (need_mask) {
-        uint32_t kw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        if (krow != nullptr) {
+      uint32_t kw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      bool keep_all = true;
+      if (krow != nullptr) {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int wi = (kbase >> 5) + w;
-            kw[w] = wi < nwords ? __ldg(krow + wi) : 0u;
-          }
+        for (int w = 0; w < 4; ++w) {
+          const int wi = (kbase >> 5) + w;
+          kw[w] = wi < nwords ? __ldg(krow + wi) : 0u;
         }
+        keep_all = (kw[0] & kw[1] & kw[2] & kw[3]) == 0xffffffffu;
+      }
+      // tiles whose 128 keys are all kept for every row of the warp skip the
+      // element-wise mask (warp-uniform choice of code path)
+      const bool need_mask = (kbase + BLOCK_N > p.Nk) || (p.causal && kbase + BLOCK_N - 1 > tile_lim) ||
+                             !__all_sync(0xffffffffu, keep_all);
+      if (need_mask) {
 #pragma unroll
         for (int c = 0; c < BLOCK_N; ++c) {
           const int key = kbase + c;

@@ -118,8 +118,9 @@ def test_key_padding_and_row_masks(fa, d):
     q, k, v = W.make_qkv(2, 3, 300, 450, d, seed=5)
     # key padding, broadcast over rows
     kp = torch.ones(2, 3, 1, 450, dtype=torch.bool)
-    kp[0, 1, 0, 200:] = False
-    kp[1, 2, 0, :130] = False
+    kp[0, 1, 0, 200:] = False      # trailing keys padded: later key tiles are skipped
+    kp[1, 2, 0, :130] = False      # leading keys masked
+    kp[0, 2, 0, :] = False         # a head with no key at all: O = 0, lse = -inf
     for causal in (False, True):
         check_full(fa, q, k, v, 0.1, causal, kp, f"keypad causal={causal}")
     # an arbitrary per-row mask, with some fully masked rows
