@@ -42,8 +42,20 @@ namespace fa {
 #ifndef FA_EMU_PAIRS_D128
 #define FA_EMU_PAIRS_D128 0
 #endif
-#ifndef FA_STAGGER
-#define FA_STAGGER 1
+#ifndef FA_STAGGER_D64
+#define FA_STAGGER_D64 1
+#endif
+#ifndef FA_STAGGER_D128
+#define FA_STAGGER_D128 0
+#endif
+#ifndef FA_SORDER
+#define FA_SORDER 1              // S_0 and S_1 are issued alternately (see the MMA issuers)
+#endif
+#ifndef FA_SUSPEND_NS
+#define FA_SUSPEND_NS 0          // suspend-time hint of the polls after a wait's first
+#endif
+#ifndef FA_EARLY_POLL
+#define FA_EARLY_POLL 1          // poll the next barriers early, use the results late
 #endif
 #ifndef FA_STAGGER_MIN_TILES
 #define FA_STAGGER_MIN_TILES 8   // only units this long amortise the delayed start
@@ -55,11 +67,18 @@ struct PrefillCfg {
   static constexpr int TILE_BYTES = BLOCK_N * D * 2;  // one Q, K or V tile (128 rows x D bf16)
   static constexpr int BOX_BYTES = 128 * 128;         // one TMA box: 128 rows x 64 bf16
   static constexpr int NBOX = D / 64;
-  static constexpr int NSLOT = (D == 128) ? 2 : 4;    // ring slots, each holding one K tile and one V tile
-  static constexpr int SLOT_BYTES = 2 * TILE_BYTES;
+  // K and V stream through separate rings. K_j is read only by S = Q K_j^T,
+  // V_j only by the later O += P V_j, so the K ring runs ahead of the V ring:
+  // K_{j+1} can land while P_j is still being computed. Both slots of key
+  // tile j are released together, by one release barrier per tile that both
+  // issuers signal once their MMAs reading tile j have completed.
+  static constexpr int NK = (D == 128) ? 3 : 4;       // K ring slots
+  static constexpr int NV = (D == 128) ? 2 : 4;       // V ring slots
+  static constexpr int NR = NK > NV ? NK : NV;        // release barriers (tile j uses j % NR)
   static constexpr int Q_OFF = 0;
-  static constexpr int KV_OFF = Q_TILES * TILE_BYTES;
-  static constexpr int BAR_OFF = KV_OFF + NSLOT * SLOT_BYTES;
+  static constexpr int K_OFF = Q_TILES * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + NK * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + NV * TILE_BYTES;
   // TMEM columns: S_0 [0,128), S_1 [128,256), O_t at O_COL + D*t; with
   // SEP_P (d = 64) P_t gets its own 64 columns at P_COL + 64*t, otherwise P_t
   // overwrites the first 64 columns of S_t.
@@ -68,9 +87,10 @@ struct PrefillCfg {
   static constexpr uint32_t P_COL = SEP_P ? O_COL + Q_TILES * D : 0;
   static constexpr uint32_t P_STRIDE = SEP_P ? BLOCK_N / 2 : BLOCK_N;
   static_assert(!SEP_P || P_COL + Q_TILES * BLOCK_N / 2 <= 512, "TMEM budget");
-  static constexpr int NBAR = 1 + 2 * NSLOT + 4 * Q_TILES + 1;
+  static constexpr int NBAR = 1 + NK + NV + NR + 4 * Q_TILES + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false);  // Q, K both K-major
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);     // V is MN-major
@@ -78,6 +98,7 @@ struct PrefillCfg {
   // FMA pipe instead of the MUFU unit, and the lazy-rescale threshold.
   static constexpr int EMU_PAIRS = (D == 64) ? FA_EMU_PAIRS_D64 : FA_EMU_PAIRS_D128;
   static constexpr float RESCALE_LOG2 = 8.0f;
+  static constexpr bool STAGGER = (D == 64) ? FA_STAGGER_D64 : FA_STAGGER_D128;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -97,11 +118,15 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 // P = 2^(s * sl2 - m) as 64 bf16 pairs in pk_all, returning the row sum of
 // the fp32 exponentials. EMU pairs of every 16 use the FMA-pipe exponential.
 // With MASKED, -inf scores give exactly 0 on both exponential paths.
+// When poll_bar is nonzero, the barrier at that shared address is polled
+// (parity poll_par) halfway through and the result left in *poll_res.
 template <bool MASKED, int EMU>
-__device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x2, uint64_t nm2, uint32_t* pk_all) {
+__device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x2, uint64_t nm2, uint32_t* pk_all,
+                                                uint32_t poll_bar, uint32_t poll_par, uint32_t* poll_res) {
   uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
   for (int ch = 0; ch < BLOCK_N / 32; ++ch) {
+    if (FA_EARLY_POLL && ch == BLOCK_N / 64 && poll_bar != 0u) *poll_res = mbar_test(poll_bar, poll_par);
     uint32_t* pk = pk_all + ch * 16;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -134,15 +159,19 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x
   return (a0 + a1) + (a2 + a3);
 }
 
-// Waits on two barriers. Both first polls are issued back to back, so when
-// both phases have already completed the thread pays one barrier round trip
-// instead of two.
+// Waits on two (three) barriers. The first polls are non-blocking and issued
+// back to back, so when every phase has already completed the thread pays
+// one barrier round trip instead of two (three). A null third barrier is
+// skipped.
 __device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t lim,
-                                           unsigned int* status, volatile int* abort) {
-  const bool ra = mbar_try_wait(smem_u32(a), pa);
-  const bool rb = mbar_try_wait(smem_u32(b), pb);
-  if (!ra && !mbar_wait(a, pa, lim, status, abort)) return false;
-  if (!rb && !mbar_wait(b, pb, lim, status, abort)) return false;
+                                           unsigned int* status, volatile int* abort, uint32_t suspend_ns,
+                                           uint64_t* c = nullptr, uint32_t pc = 0) {
+  const uint32_t ra = mbar_test(smem_u32(a), pa);
+  const uint32_t rb = mbar_test(smem_u32(b), pb);
+  const uint32_t rc = c == nullptr ? 1u : mbar_test(smem_u32(c), pc);
+  if (!ra && !mbar_wait(a, pa, lim, status, abort, suspend_ns)) return false;
+  if (!rb && !mbar_wait(b, pb, lim, status, abort, suspend_ns)) return false;
+  if (!rc && !mbar_wait(c, pc, lim, status, abort, suspend_ns)) return false;
   return true;
 }
 
@@ -151,16 +180,18 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using C = PrefillCfg<D>;
-  constexpr int NSLOT = C::NSLOT;
+  constexpr int NK = C::NK, NV = C::NV, NR = C::NR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::Q_OFF;
-  uint8_t* sKV = smem + C::KV_OFF;
+  uint8_t* sK = smem + C::K_OFF;
+  uint8_t* sV = smem + C::V_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars;
-  uint64_t* full = bars + 1;
-  uint64_t* empty = full + NSLOT;
-  uint64_t* s_full = empty + NSLOT;
+  uint64_t* full_k = bars + 1;      // K_j landed in slot j % NK
+  uint64_t* full_v = full_k + NK;   // V_j landed in slot j % NV
+  uint64_t* rel = full_v + NV;      // both issuers are done with key tile j (j % NR)
+  uint64_t* s_full = rel + NR;
   uint64_t* p_full = s_full + Q_TILES;
   uint64_t* o_done = p_full + Q_TILES;
   uint64_t* s_free = o_done + Q_TILES;
@@ -211,10 +242,9 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < NSLOT; ++i) {
-      mbar_init(full + i, 1);
-      mbar_init(empty + i, Q_TILES);  // released by both MMA-issuing warps
-    }
+    for (int i = 0; i < NK; ++i) mbar_init(full_k + i, 1);
+    for (int i = 0; i < NV; ++i) mbar_init(full_v + i, 1);
+    for (int i = 0; i < NR; ++i) mbar_init(rel + i, Q_TILES);  // both MMA-issuing warps
     for (int t = 0; t < Q_TILES; ++t) {
       mbar_init(s_full + t, 1);
       mbar_init(p_full + t, 128);
@@ -256,27 +286,39 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           for (int b = 0; b < C::NBOX; ++b)
             tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full, 64 * b, rq + t * BLOCK_M, bh);
       }
-      int nl = 0;  // number of K/V tiles loaded so far (ring position)
+      // Tile jj goes to K slot jj % NK once tile jj - NK was released, and to
+      // V slot jj % NV once tile jj - NV was released (release of tile i is
+      // phase i / NR of rel[i % NR]).
+      auto wait_rel = [&](int i) -> bool {
+        if (i < 0) return true;
+        const bool w = mbar_wait(rel + (i % NR), static_cast<uint32_t>((i / NR) & 1), lim, p.status, abort_flag, FA_SUSPEND_NS);
+        return __all_sync(0xffffffffu, w) != 0;
+      };
+      int nlk = 0, nlv = 0;  // K / V tiles loaded so far
       bool ok = true;
       for (int jj = 0; ok && jj < n_max; ++jj) {
-        const int slot = jj % NSLOT;
-        ok = mbar_wait(empty + slot, ((jj / NSLOT) & 1) ^ 1, lim, p.status, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+        if (!(ok = wait_rel(jj - NK))) break;
         if (leader) {
-          uint8_t* dst = sKV + slot * C::SLOT_BYTES;
-          mbar_arrive_expect_tx(full + slot, C::SLOT_BYTES);
+          uint8_t* dst = sK + (jj % NK) * C::TILE_BYTES;
+          mbar_arrive_expect_tx(full_k + (jj % NK), C::TILE_BYTES);
           for (int b = 0; b < C::NBOX; ++b)
-            tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full + slot, 64 * b, jj * BLOCK_N, bh);
-          for (int b = 0; b < C::NBOX; ++b)
-            tma_load_3d(dst + C::TILE_BYTES + b * C::BOX_BYTES, &tmV, full + slot, 64 * b, jj * BLOCK_N, bh);
+            tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full_k + (jj % NK), 64 * b, jj * BLOCK_N, bh);
         }
-        ++nl;
+        ++nlk;
+        if (!(ok = wait_rel(jj - NV))) break;
+        if (leader) {
+          uint8_t* dst = sV + (jj % NV) * C::TILE_BYTES;
+          mbar_arrive_expect_tx(full_v + (jj % NV), C::TILE_BYTES);
+          for (int b = 0; b < C::NBOX; ++b)
+            tma_load_3d(dst + b * C::BOX_BYTES, &tmV, full_v + (jj % NV), 64 * b, jj * BLOCK_N, bh);
+        }
+        ++nlv;
       }
       if (!ok && leader) {
         // error path: let the copies already issued land before the CTA exits
         mbar_wait_drain(q_full, 0, lim);
-        for (int n = max(0, nl - NSLOT); n < nl; ++n) mbar_wait_drain(full + (n % NSLOT), (n / NSLOT) & 1, lim);
+        for (int n = max(0, nlk - NK); n < nlk; ++n) mbar_wait_drain(full_k + (n % NK), (n / NK) & 1, lim);
+        for (int n = max(0, nlv - NV); n < nlv; ++n) mbar_wait_drain(full_v + (n % NV), (n / NV) & 1, lim);
       }
       __syncwarp();
     } else if (warp == PREFILL_MMA_WARP0 || warp == PREFILL_MMA_WARP0 + 1) {
@@ -288,88 +330,111 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       // The whole warp runs the loop and waits; lane 0 issues MMAs and commits.
       const int t = warp - PREFILL_MMA_WARP0;
       const bool leader = lane == 0;
-      bool ok = mbar_wait(q_full, 0, lim, p.status, abort_flag);
+      bool ok = mbar_wait(q_full, 0, lim, p.status, abort_flag, FA_SUSPEND_NS);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
       const uint32_t sQa = smem_u32(sQ) + t * C::TILE_BYTES;
-      const uint32_t sKVa = smem_u32(sKV);
-      // descriptors for ring slot 0; other slots differ only in the start-address
-      // field (bits 0-13, address >> 4)
-      uint64_t dq[D / 16], dk[D / 16], dv[BLOCK_N / 16];
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-        dq[kk] = sdesc_sw128(sQa + off, 16, 1024);
-        dk[kk] = sdesc_sw128(sKVa + off, 16, 1024);
-      }
-#pragma unroll
-      for (int kk = 0; kk < BLOCK_N / 16; ++kk) dv[kk] = sdesc_sw128(sKVa + kk * 2048, C::BOX_BYTES, 1024);
+      const uint32_t sKa = smem_u32(sK);
+      const uint32_t sVa = smem_u32(sV);
+      // Low descriptor words of Q_t, K slot 0 and V slot 0 (every operand
+      // shares the high word: 1024-byte 8-row groups, 128-byte swizzle). The
+      // K-step kk of Q and K (K-major) starts (kk / 4) boxes plus (kk % 4) x 32
+      // bytes in; that of V (MN-major, 64-column boxes LBO apart) 16 rows =
+      // 2048 bytes in. Another ring slot adds its offset to the low word.
+      constexpr uint32_t DHI = sdesc_sw128_hi(1024);
+      const uint32_t q_lo = sdesc_sw128_lo(sQa, 16);
+      const uint32_t k_lo = sdesc_sw128_lo(sKa, 16);
+      const uint32_t v_lo = sdesc_sw128_lo(sVa, C::BOX_BYTES);
       const int nt = n_t[t];
       const uint32_t dS = tmem + BLOCK_N * t;
       const uint32_t dO = tmem + C::O_COL + D * t;
       const uint32_t aP = tmem + C::P_COL + C::P_STRIDE * t;
 
       auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
-        ok = mbar_wait(bar, parity, lim, p.status, abort_flag);
+        ok = mbar_wait(bar, parity, lim, p.status, abort_flag, FA_SUSPEND_NS);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         return ok;
       };
-      auto wait_bar2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb) {
-        ok = mbar_wait2(a, pa, b, pb, lim, p.status, abort_flag);
+      auto wait_bar2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t* c = nullptr,
+                           uint32_t pc = 0) {
+        ok = mbar_wait2(a, pa, b, pb, lim, p.status, abort_flag, FA_SUSPEND_NS, c, pc);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         return ok;
       };
-      auto full_bar = [&](int jj) { return full + (jj % NSLOT); };
-      auto full_par = [&](int jj) { return static_cast<uint32_t>((jj / NSLOT) & 1); };
+      auto fk_bar = [&](int jj) { return full_k + (jj % NK); };
+      auto fk_par = [&](int jj) { return static_cast<uint32_t>((jj / NK) & 1); };
+      auto fv_bar = [&](int jj) { return full_v + (jj % NV); };
+      auto fv_par = [&](int jj) { return static_cast<uint32_t>((jj / NV) & 1); };
       auto issue_s = [&](int jj) {  // S_t = Q_t K_jj^T
         if (leader) {
-          const uint64_t kadd = static_cast<uint64_t>(((jj % NSLOT) * C::SLOT_BYTES) >> 4);
+          const uint32_t kb = k_lo + static_cast<uint32_t>(((jj % NK) * C::TILE_BYTES) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) mma_ss(dS, dq[kk], dk[kk] + kadd, C::IDESC_S, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+            mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, C::IDESC_S, kk > 0 ? 1u : 0u);
+          }
           mma_commit(s_full + t);
         }
       };
       auto issue_pv = [&](int jj) {  // O_t (+)= P_t V_jj
         if (leader) {
-          const uint64_t vadd = static_cast<uint64_t>(((jj % NSLOT) * C::SLOT_BYTES + C::TILE_BYTES) >> 4);
+          const uint32_t vb = v_lo + static_cast<uint32_t>(((jj % NV) * C::TILE_BYTES) >> 4);
 #pragma unroll
           for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-            mma_ts(dO, aP + kk * 8, dv[kk] + vadd, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_w(dO, aP + kk * 8, vb + kk * (2048 >> 4), DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
           mma_commit(o_done + t);
         }
       };
-      // A slot is released by both issuers (the empty barrier counts 2): by a
-      // commit when this warp's MMAs read it, by a plain arrive when they did
-      // not (a tile whose range ended or is empty). A commit from a thread with
-      // no tcgen05 operation to track is not relied on to arrive. An unused
-      // slot is first waited for (full), so the arrive lands in that load's
+      // Key tile jj is released by both issuers (rel counts 2): by a commit
+      // when this warp's MMAs read it, by a plain arrive when they did not (a
+      // tile past this Q tile's range). A commit from a thread with no tcgen05
+      // operation to track is not relied on to arrive. An unused tile is first
+      // waited for (both loads landed), so the arrive lands in that tile's
       // phase: an idle warp must not run around the ring ahead of the loads.
       auto release = [&](int jj, bool used) {
-        if (!used && !wait_bar(full_bar(jj), full_par(jj))) return;
+        if (!used && !wait_bar2(fk_bar(jj), fk_par(jj), fv_bar(jj), fv_par(jj))) return;
         if (leader) {
-          if (used) mma_commit(empty + (jj % NSLOT));
-          else mbar_arrive(empty + (jj % NSLOT));
+          if (used) mma_commit(rel + (jj % NR));
+          else mbar_arrive(rel + (jj % NR));
         }
       };
+
+      // The two tiles' score MMAs alternate: S_{0,j} is issued only after
+      // S_{1,j-1} has completed and S_{1,j} only after S_{0,j} has completed
+      // (while both tiles still have key tiles). Without this order nothing
+      // keeps the tiles half a period apart, and they drift into lockstep:
+      // both score MMAs share the tensor pipe at once and then both softmax
+      // warpgroups share the SM's exponential units at once. The chain of
+      // waits also keeps each parity wait on the other tile's s_full
+      // unambiguous (that barrier is at most one phase behind or ahead).
+      // (barrier, parity) that S_{t,jj} must wait for, or null
+      auto order_bar = [&](int jj) -> uint64_t* {
+        if (!FA_SORDER) return nullptr;
+        if (t == 0) return (jj >= 1 && jj - 1 < n_t[1]) ? s_full + 1 : nullptr;
+        return (jj < n_t[0]) ? s_full + 0 : nullptr;
+      };
+      auto order_par = [&](int jj) -> uint32_t { return static_cast<uint32_t>((t == 0 ? jj - 1 : jj) & 1); };
 
       // Ping-pong: the second Q tile starts once the first tile's first
       // softmax is done, so one tile's exponentials overlap the other tile's
       // MMAs instead of both tiles competing for the same unit at once.
-      if (FA_STAGGER && t == 1 && n_t[0] >= FA_STAGGER_MIN_TILES && nt > 0) wait_bar(p_full + 0, 0);
+      if (C::STAGGER && t == 1 && n_t[0] >= FA_STAGGER_MIN_TILES && nt > 0) wait_bar(p_full + 0, 0);
 
       if (C::SEP_P) {
         // Software pipeline: S_{j+1} is issued as soon as the softmax has read
         // S_j (s_free), so the next scores are computed while it exponentiates.
-        if (ok && nt > 0 && wait_bar(full_bar(0), full_par(0))) issue_s(0);
+        if (ok && nt > 0 && wait_bar2(fk_bar(0), fk_par(0), fk_bar(0), fk_par(0), order_bar(0), order_par(0)))
+          issue_s(0);
         for (int jj = 0; ok && jj < n_max; ++jj) {
           if (jj + 1 < nt) {
-            if (!wait_bar2(full_bar(jj + 1), full_par(jj + 1), s_free + t, jj & 1)) break;
+            if (!wait_bar2(fk_bar(jj + 1), fk_par(jj + 1), s_free + t, jj & 1, order_bar(jj + 1), order_par(jj + 1)))
+              break;
             issue_s(jj + 1);
           }
           if (jj < nt) {
-            if (!wait_bar(p_full + t, jj & 1)) break;
+            if (!wait_bar2(p_full + t, jj & 1, fv_bar(jj), fv_par(jj))) break;
             issue_pv(jj);
           }
           release(jj, jj < nt);
@@ -379,11 +444,13 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         // (which reads P_{t,j-1} from the same columns) has completed.
         for (int jj = 0; ok && jj < n_max; ++jj) {
           if (jj < nt) {
-            const bool w = (jj > 0) ? wait_bar2(full_bar(jj), full_par(jj), o_done + t, (jj - 1) & 1)
-                                    : wait_bar(full_bar(jj), full_par(jj));
+            const bool w = (jj > 0) ? wait_bar2(fk_bar(jj), fk_par(jj), o_done + t, (jj - 1) & 1, order_bar(jj),
+                                                order_par(jj))
+                                    : wait_bar2(fk_bar(jj), fk_par(jj), fk_bar(jj), fk_par(jj), order_bar(jj),
+                                                order_par(jj));
             if (!w) break;
             issue_s(jj);
-            if (!wait_bar(p_full + t, jj & 1)) break;
+            if (!wait_bar2(p_full + t, jj & 1, fv_bar(jj), fv_par(jj))) break;
             issue_pv(jj);
           }
           release(jj, jj < nt);
@@ -425,10 +492,19 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     bool ok = true;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
 
+    // Barrier polls are issued early and their results used late (a poll on a
+    // completed barrier still costs a shared-memory round trip, long while the
+    // tensor core streams operands from shared memory): s_full of the next key
+    // tile right after P is stored, o_done of the previous PV halfway through
+    // the exponentials. A poll that finds the phase incomplete falls back to
+    // the bounded wait.
+    uint32_t s_ready = 0;
     for (int j = 0; j < n; ++j) {
-      ok = mbar_wait(s_full + t, j & 1, lim, p.status, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, s_ready)) {
+        ok = mbar_wait(s_full + t, j & 1, lim, p.status, abort_flag, FA_SUSPEND_NS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
       tc_fence_after();
       uint32_t s[BLOCK_N];
       tmem_ld32(tS + 0, s);
@@ -489,18 +565,27 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const uint64_t nm2 = f2pack(-m_use, -m_use);
       uint32_t pk[BLOCK_N / 2];
-      const float rowsum = need_mask ? softmax_tile_p<true, C::EMU_PAIRS>(s, sl2x2, nm2, pk)
-                                     : softmax_tile_p<false, C::EMU_PAIRS>(s, sl2x2, nm2, pk);
+      uint32_t o_ready = 0;
+      const uint32_t o_poll = (C::SEP_P && j > 0) ? smem_u32(o_done + t) : 0u;
+      const uint32_t o_par = static_cast<uint32_t>((j - 1) & 1);
+      // (with no FMA-pipe pairs both instantiations are the same code: keep
+      // one copy of the unrolled loop in the instruction cache)
+      const float rowsum = (C::EMU_PAIRS > 0 && need_mask)
+                               ? softmax_tile_p<true, C::EMU_PAIRS>(s, sl2x2, nm2, pk, o_poll, o_par, &o_ready)
+                               : softmax_tile_p<false, C::EMU_PAIRS>(s, sl2x2, nm2, pk, o_poll, o_par, &o_ready);
       if (C::SEP_P && j > 0) {
         // P_t and O_t are free once PV_{t,j-1} has completed; it ran while
         // the exponentials above were computed
-        ok = mbar_wait(o_done + t, (j - 1) & 1, lim, p.status, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, o_ready)) {
+          ok = mbar_wait(o_done + t, (j - 1) & 1, lim, p.status, abort_flag, FA_SUSPEND_NS);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
         tc_fence_after();
       }
       tmem_st32(tP, pk);
       tmem_st32(tP + 32, pk + 32);
+      s_ready = (FA_EARLY_POLL && j + 1 < n) ? mbar_test(smem_u32(s_full + t), (j + 1) & 1) : 0u;
       l = fmaf(l, alpha, rowsum);
       // O_t is quiescent here: PV_{t,j-1} has completed (waited above, or before
       // S_{t,j} was issued) and PV_{t,j} waits for p_full.
@@ -529,7 +614,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 
     // ---- epilogue: O = o / l (0 for an empty row), lse = m + ln l (-inf for an empty row)
     if (ok && n > 0) {
-      ok = mbar_wait(o_done + t, (n - 1) & 1, lim, p.status, abort_flag);
+      ok = mbar_wait(o_done + t, (n - 1) & 1, lim, p.status, abort_flag, FA_SUSPEND_NS);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
     }
