@@ -94,7 +94,8 @@ fa_status device_state(DeviceState** out) {
 }
 
 // 3-D bf16 tensor map over [BH, rows, d] with 128-row x 64-column boxes and
-// 128-byte swizzle; rows past `rows` read as zeros.
+// 128-byte swizzle; rows past `rows` read as zeros (loads) or are not written
+// (stores).
 fa_status encode_map(CUtensorMap* map, const void* base, int rows, int BH, int d) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
@@ -166,8 +167,9 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
 
   DeviceState* st = nullptr;
   if (fa_status s = device_state(&st)) return s;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (fa_status s = encode_map(&tq, q, Nq, static_cast<int>(BH), d)) return s;
+  if (fa_status s = encode_map(&to, o, Nq, static_cast<int>(BH), d)) return s;
   if (fa_status s = encode_map(&tk, k, Nk, static_cast<int>(BH), d)) return s;
   if (fa_status s = encode_map(&tv, v, Nk, static_cast<int>(BH), d)) return s;
 
@@ -190,7 +192,7 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
   p.scale_log2 = fmaxf(scale * 1.4426950408889634f, 1.17549435e-38f);
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
-  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   t_launches += 1;
   return FA_OK;

@@ -59,7 +59,7 @@ struct DecodeParams {
 
 // Launchers (defined next to their kernels). Return a CUDA error code.
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, cudaStream_t stream);
+                           const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream);
 size_t prefill_smem_bytes(int d);
 cudaError_t prefill_set_attributes(int d);
 int prefill_num_regs(int d);   // registers per thread the prefill kernel launches with

@@ -178,7 +178,8 @@ __device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b
 template <int D>
 __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                      const PrefillParams p) {
   using C = PrefillCfg<D>;
   constexpr int NK = C::NK, NV = C::NV, NR = C::NR;
   extern __shared__ uint8_t smem_raw[];
@@ -280,6 +281,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
         const int rq = pair * (Q_TILES * BLOCK_M);
         mbar_arrive_expect_tx(q_full, Q_TILES * C::TILE_BYTES);
         for (int t = 0; t < Q_TILES; ++t)
@@ -613,14 +615,22 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     }
 
     // ---- epilogue: O = o / l (0 for an empty row), lse = m + ln l (-inf for an empty row)
-    if (ok && n > 0) {
-      ok = mbar_wait(o_done + t, (n - 1) & 1, lim, p.status, abort_flag, FA_SUSPEND_NS);
+    // O goes through shared memory into one TMA store per 64-column box. The
+    // staging buffer is this tile's Q tile: every S MMA that read it has
+    // completed once the last PV has (the issuer's commit covers all its
+    // earlier MMAs); a tile with no key tile ran no MMA, so there the Q load
+    // itself is waited for. Rows are written in the 128-byte-swizzled layout
+    // the tensor map expects; rows past Nq are clipped by the store.
+    if (ok) {
+      ok = (n > 0) ? mbar_wait(o_done + t, (n - 1) & 1, lim, p.status, abort_flag, FA_SUSPEND_NS)
+                   : mbar_wait(q_full, 0, lim, p.status, abort_flag, FA_SUSPEND_NS);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
     }
+    uint8_t* sO = sQ + t * C::TILE_BYTES;
     if (ok) {
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.Nq + qi) * D;
+      const uint32_t srow = smem_u32(sO) + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
@@ -634,16 +644,25 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
-        if (qi < p.Nq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) {
+          const int c = ch * 4 + v;  // 16-byte chunk of the row: box c / 8, chunk c % 8 of the box
+          const uint32_t a = srow + static_cast<uint32_t>((c >> 3) * C::BOX_BYTES) +
+                             (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4);
+          st_shared_v4(a, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (p.lse != nullptr && qi < p.Nq)
         p.lse[static_cast<size_t>(bh) * p.Nq + qi] =
             (l > 0.f) ? (m + lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + t, 128);  // every thread of the tile, on every path
+    if (wq == 0 && lane == 0 && r0 < p.Nq && *abort_flag == 0) {
+#pragma unroll
+      for (int b = 0; b < C::NBOX; ++b) tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
+      bulk_commit_group();
+      bulk_wait_group_all();
     }
   }
 
@@ -657,10 +676,10 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 
 template <int D>
 static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                    const PrefillParams& p, cudaStream_t stream) {
+                                    const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
   const long long units = static_cast<long long>(p.n_qpairs) * p.B * p.H;
   fa_prefill_kernel<D><<<static_cast<unsigned>(units), PREFILL_THREADS, PrefillCfg<D>::SMEM, stream>>>(tq, tk, tv,
-                                                                                                      p);
+                                                                                                      to, p);
   return cudaGetLastError();
 }
 
@@ -684,8 +703,8 @@ cudaError_t prefill_set_attributes(int d) {
 }
 
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, cudaStream_t stream) {
-  return d == 64 ? launch_prefill_t<64>(tq, tk, tv, p, stream) : launch_prefill_t<128>(tq, tk, tv, p, stream);
+                           const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
+  return d == 64 ? launch_prefill_t<64>(tq, tk, tv, to, p, stream) : launch_prefill_t<128>(tq, tk, tv, to, p, stream);
 }
 
 }  // namespace fa
