@@ -41,6 +41,7 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 struct DeviceState {
   bool ready = false;
   unsigned int* status = nullptr;
+  int num_sms = 0;
 };
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
@@ -65,6 +66,8 @@ fa_status device_state(DeviceState** out) {
     if (major != 10 || minor != 3)
       return fail(FA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
                   minor);
+    if ((e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(multiprocessors)");
     void* p = nullptr;
     if ((e = cudaGetSymbolAddress(&p, fa::g_device_status)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status)");
@@ -192,6 +195,7 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
   p.scale_log2 = fmaxf(scale * 1.4426950408889634f, 1.17549435e-38f);
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
+  p.max_ctas = st->num_sms;
   cudaError_t e = fa::launch_prefill(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   t_launches += 1;

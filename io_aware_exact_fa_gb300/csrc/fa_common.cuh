@@ -27,10 +27,28 @@ constexpr int PREFILL_MMA_WARP0 = 9;       // warps 9, 10 issue MMAs (one per Q 
 // PREFILL_LAUNCH_REGS; each SM sub-partition holds one warp of every
 // warpgroup, so 2 * SOFTMAX + PRODUCER must not exceed 3 * PREFILL_LAUNCH_REGS.
 constexpr int PREFILL_LAUNCH_REGS = 168;
-constexpr int PREFILL_SOFTMAX_REGS = 224;
-constexpr int PREFILL_PRODUCER_REGS = 56;
-static_assert(2 * PREFILL_SOFTMAX_REGS + PREFILL_PRODUCER_REGS <= 3 * PREFILL_LAUNCH_REGS,
-              "setmaxnreg split exceeds the registers the launch provides");
+#ifndef FA_SOFTMAX_REGS_D64
+#define FA_SOFTMAX_REGS_D64 224
+#endif
+#ifndef FA_SOFTMAX_REGS_D128
+#define FA_SOFTMAX_REGS_D128 216
+#endif
+// registers of the softmax warpgroups and of the producer/MMA warpgroup after
+// setmaxnreg, per head dimension (the d = 128 MMA issuers keep more state)
+__host__ __device__ constexpr int prefill_softmax_regs(int d) {
+  return d == 64 ? FA_SOFTMAX_REGS_D64 : FA_SOFTMAX_REGS_D128;
+}
+__host__ __device__ constexpr int prefill_producer_regs(int d) {
+  return 3 * PREFILL_LAUNCH_REGS - 2 * prefill_softmax_regs(d) < 256 ? 3 * PREFILL_LAUNCH_REGS - 2 * prefill_softmax_regs(d)
+                                                                      : 256;
+}
+static_assert(2 * prefill_softmax_regs(64) + prefill_producer_regs(64) <= 3 * PREFILL_LAUNCH_REGS &&
+                  2 * prefill_softmax_regs(128) + prefill_producer_regs(128) <= 3 * PREFILL_LAUNCH_REGS,
+              "setmaxnreg split exceeds the launch allocation");
+static_assert(prefill_softmax_regs(64) % 8 == 0 && prefill_softmax_regs(128) % 8 == 0 &&
+                  prefill_producer_regs(64) % 8 == 0 && prefill_producer_regs(128) % 8 == 0 &&
+                  prefill_producer_regs(64) >= 24 && prefill_producer_regs(128) >= 24,
+              "setmaxnreg counts are multiples of 8 in [24, 256]");
 
 struct PrefillParams {
   void* o;                   // bf16 [B*H, Nq, d]
@@ -43,6 +61,7 @@ struct PrefillParams {
   float scale_log2;          // scale * log2(e)
   uint64_t wait_limit_ns;
   unsigned int* status;      // device status word
+  int max_ctas;              // CTAs of a persistent launch (the SM count)
 };
 
 struct DecodeParams {

@@ -63,33 +63,16 @@ __device__ __forceinline__ uint32_t mbar_test(uint32_t bar, uint32_t parity) {
   return ok;
 }
 
-// try_wait with a suspend-time hint: a thread whose phase has not completed
-// may be suspended up to `ns` nanoseconds (woken earlier when it completes)
-// instead of returning at once and re-polling.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait until the phase with parity `parity` of `bar` has completed. Gives up
 // after `limit_ns` of polling, or as soon as another role of the CTA raised
 // `*abort`; on giving up it sets *abort, records the timeout and returns false.
-// A nonzero `suspend_ns` is passed to the polls after the first as the
-// suspend-time hint.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                          unsigned int* status, volatile int* abort, uint32_t suspend_ns = 0) {
+                                          unsigned int* status, volatile int* abort) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (suspend_ns ? mbar_try_wait_hint(a, parity, suspend_ns) : mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait(a, parity)) return true;
     if ((i & 31u) == 0u) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -129,6 +112,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Waits until the shared memory read by this thread's bulk groups may be reused.
+__device__ __forceinline__ void bulk_wait_group_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {

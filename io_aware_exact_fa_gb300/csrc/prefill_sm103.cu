@@ -12,23 +12,30 @@
 // of "FlashAttention: Attention Is Limited by Memory, Not Math" describes as
 // parallel over sequence length).
 //
-// One CTA per SM handles a work unit of two 128-row Q tiles of one (b, h).
+// A work unit is two 128-row Q tiles of one (b, h). The launch is persistent:
+// one CTA per SM walks its share of the units (round robin; causal units,
+// sorted longest first, in snake order), and every barrier phase runs on
+// across units, so the next unit's loads and first MMAs overlap the current
+// unit's last steps and epilogue.
 // 384 threads = 3 warpgroups; after set-up the softmax warpgroups take more
 // registers and the producer warpgroup fewer (setmaxnreg).
-//   warp 8      TMA producer: Q once, then K_j / V_j into a ring of slots.
+//   warp 8      TMA producer for K_j / V_j, into separate rings of slots.
 //   warp 9      TMEM allocator; with warp 10, MMA issuers (one per Q tile):
 //               S_t = Q_t K_j^T into TMEM, later O_t += P_t V_j.
-//   warp 11     idle after set-up.
+//   warp 11     TMA producer for Q (one tile per buffer per unit).
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: each thread
 //               owns one query row (TMEM lane), reads its 128 scores with
 //               tcgen05.ld, applies the mask from absolute positions, folds
-//               the tile into (m, l), writes P (bf16) over S in TMEM and
-//               rescales its O row when the running max rose; at the end it
-//               divides by l and writes O (bf16) and lse (fp32).
+//               the tile into (m, l), writes P (bf16) to TMEM and rescales
+//               its O row when the running max rose; at the end it divides by
+//               l and writes O (bf16, through a TMA store) and lse (fp32).
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
 // The two Q tiles ping-pong: while one softmax warpgroup works, the tensor
 // core runs the other tile's MMAs.
 #include <cuda_bf16.h>
+
+#include <algorithm>
+#include <climits>
 
 #include "fa_ptx.cuh"
 
@@ -51,11 +58,17 @@ namespace fa {
 #ifndef FA_SORDER
 #define FA_SORDER 1              // S_0 and S_1 are issued alternately (see the MMA issuers)
 #endif
-#ifndef FA_SUSPEND_NS
-#define FA_SUSPEND_NS 0          // suspend-time hint of the polls after a wait's first
-#endif
 #ifndef FA_EARLY_POLL
 #define FA_EARLY_POLL 1          // poll the next barriers early, use the results late
+#endif
+#ifndef FA_PERSIST_D64
+#define FA_PERSIST_D64 1         // one CTA per SM walking many units (else one CTA per unit)
+#endif
+#ifndef FA_PERSIST_D128
+#define FA_PERSIST_D128 0
+#endif
+#ifndef FA_O_STAGE
+#define FA_O_STAGE 1             // separate O staging buffers where shared memory allows (d = 64)
 #endif
 #ifndef FA_STAGGER_MIN_TILES
 #define FA_STAGGER_MIN_TILES 8   // only units this long amortise the delayed start
@@ -78,7 +91,12 @@ struct PrefillCfg {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_TILES * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + NK * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + NV * TILE_BYTES;
+  // At d = 64 the epilogue stages O in buffers of its own, so the next unit's
+  // Q may be loaded as soon as this unit's score MMAs are done; at d = 128
+  // there is no room and O is staged in the Q buffer.
+  static constexpr bool O_STAGE = (D == 64) && FA_O_STAGE;
+  static constexpr int O_OFF = V_OFF + NV * TILE_BYTES;
+  static constexpr int BAR_OFF = O_OFF + (O_STAGE ? Q_TILES * TILE_BYTES : 0);
   // TMEM columns: S_0 [0,128), S_1 [128,256), O_t at O_COL + D*t; with
   // SEP_P (d = 64) P_t gets its own 64 columns at P_COL + 64*t, otherwise P_t
   // overwrites the first 64 columns of S_t.
@@ -87,7 +105,7 @@ struct PrefillCfg {
   static constexpr uint32_t P_COL = SEP_P ? O_COL + Q_TILES * D : 0;
   static constexpr uint32_t P_STRIDE = SEP_P ? BLOCK_N / 2 : BLOCK_N;
   static_assert(!SEP_P || P_COL + Q_TILES * BLOCK_N / 2 <= 512, "TMEM budget");
-  static constexpr int NBAR = 1 + NK + NV + NR + 4 * Q_TILES + 1;
+  static constexpr int NBAR = 6 * Q_TILES + NK + NV + NR + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -99,6 +117,11 @@ struct PrefillCfg {
   static constexpr int EMU_PAIRS = (D == 64) ? FA_EMU_PAIRS_D64 : FA_EMU_PAIRS_D128;
   static constexpr float RESCALE_LOG2 = 8.0f;
   static constexpr bool STAGGER = (D == 64) ? FA_STAGGER_D64 : FA_STAGGER_D128;
+  // Persistent launch where it measured faster: at d = 64, where the next
+  // unit's Q loads while the current unit finishes (separate O staging). At
+  // d = 128 the Q buffer also stages O, so the next Q waits for the epilogue
+  // and one CTA per unit is faster.
+  static constexpr bool PERSIST = (D == 64) ? FA_PERSIST_D64 : FA_PERSIST_D128;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -164,15 +187,53 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x
 // one barrier round trip instead of two (three). A null third barrier is
 // skipped.
 __device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t lim,
-                                           unsigned int* status, volatile int* abort, uint32_t suspend_ns,
-                                           uint64_t* c = nullptr, uint32_t pc = 0) {
+                                           unsigned int* status, volatile int* abort, uint64_t* c = nullptr,
+                                           uint32_t pc = 0) {
   const uint32_t ra = mbar_test(smem_u32(a), pa);
   const uint32_t rb = mbar_test(smem_u32(b), pb);
   const uint32_t rc = c == nullptr ? 1u : mbar_test(smem_u32(c), pc);
-  if (!ra && !mbar_wait(a, pa, lim, status, abort, suspend_ns)) return false;
-  if (!rb && !mbar_wait(b, pb, lim, status, abort, suspend_ns)) return false;
-  if (!rc && !mbar_wait(c, pc, lim, status, abort, suspend_ns)) return false;
+  if (!ra && !mbar_wait(a, pa, lim, status, abort)) return false;
+  if (!rb && !mbar_wait(b, pb, lim, status, abort)) return false;
+  if (!rc && !mbar_wait(c, pc, lim, status, abort)) return false;
   return true;
+}
+
+// Work unit u (0 <= u < BH * n_qpairs): Q-tile pair `pair` of head `bh`.
+// Causal runs the longest pairs first.
+struct Unit {
+  int bh, pair, n0, n1;  // n_t: key tiles Q tile t visits
+};
+__device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u, int kv_keep) {
+  const int BH = p.B * p.H;
+  Unit w;
+  w.pair = p.causal ? (p.n_qpairs - 1 - u / BH) : (u / BH);
+  w.bh = u % BH;
+  const int nkv_total = (p.Nk + BLOCK_N - 1) / BLOCK_N;
+  int n[Q_TILES];
+#pragma unroll
+  for (int t = 0; t < Q_TILES; ++t) {
+    const int r0 = w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M;
+    int nt = 0;
+    if (r0 < p.Nq) {
+      if (p.causal) {
+        // bottom-right alignment: row i sees keys j <= i + (Nk - Nq)
+        const int last_key = min(r0 + BLOCK_M - 1, p.Nq - 1) + (p.Nk - p.Nq);
+        nt = last_key < 0 ? 0 : min(nkv_total, last_key / BLOCK_N + 1);
+      } else {
+        nt = nkv_total;
+      }
+    }
+    n[t] = min(nt, kv_keep);
+  }
+  w.n0 = n[0];
+  w.n1 = n[1];
+  return w;
+}
+// The k-th unit of CTA c of G, or a value >= U when it has no k-th unit.
+// Round robin; with `snake` every other round runs in reverse CTA order, so
+// with units sorted longest first the per-CTA sums stay balanced.
+__device__ __forceinline__ int unit_of(int c, int k, int G, bool snake) {
+  return k * G + ((snake && (k & 1)) ? (G - 1 - c) : c);
 }
 
 template <int D>
@@ -188,48 +249,36 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   uint8_t* sK = smem + C::K_OFF;
   uint8_t* sV = smem + C::V_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* q_full = bars;
-  uint64_t* full_k = bars + 1;      // K_j landed in slot j % NK
-  uint64_t* full_v = full_k + NK;   // V_j landed in slot j % NV
-  uint64_t* rel = full_v + NV;      // both issuers are done with key tile j (j % NR)
-  uint64_t* s_full = rel + NR;
-  uint64_t* p_full = s_full + Q_TILES;
-  uint64_t* o_done = p_full + Q_TILES;
-  uint64_t* s_free = o_done + Q_TILES;
-  uint64_t* drain = s_free + Q_TILES;
+  uint64_t* q_full = bars;                 // Q_t of unit k landed (phase k)
+  uint64_t* q_free = q_full + Q_TILES;     // Q_t buffer free again after unit k (phase k): its score
+                                           // MMAs are done (O_STAGE) or its O store read it
+  uint64_t* full_k = q_free + Q_TILES;     // K of key tile g landed in slot g % NK
+  uint64_t* full_v = full_k + NK;          // V of key tile g landed in slot g % NV
+  uint64_t* rel = full_v + NV;             // both issuers are done with key tile g (g % NR)
+  uint64_t* s_full = rel + NR;             // S_t of step c complete (per-tile step count c)
+  uint64_t* p_full = s_full + Q_TILES;     // P_t of step c stored
+  uint64_t* o_done = p_full + Q_TILES;     // PV_t of step c complete
+  uint64_t* s_free = o_done + Q_TILES;     // S_t of step c read by the softmax
+  uint64_t* unit_done = s_free + Q_TILES;  // both issuers finished unit k (phase k)
+  uint64_t* drain = unit_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  int* kv_keep_slot = reinterpret_cast<int*>(smem + C::MISC_OFF + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
+  const int U = p.B * p.H * p.n_qpairs;
+  const int G = static_cast<int>(gridDim.x);
+  const int cta = static_cast<int>(blockIdx.x);
+  const bool snake = p.causal != 0;
+  // With one key mask broadcast over the rows of a head, key tiles after the
+  // last one with any key kept are skipped by every role; the host then
+  // launches one CTA per unit and warp 11 finds that tile before set-up ends.
+  const bool trim = p.keep != nullptr && p.msq == 0;
 
-  // ---- work unit: Q-tile pair `pair` of head `bh`; causal runs the longest pairs first
-  const int BH = p.B * p.H;
-  const int unit = blockIdx.x;
-  const int pair = p.causal ? (p.n_qpairs - 1 - unit / BH) : (unit / BH);
-  const int bh = unit % BH;
-  const int nkv_total = (p.Nk + BLOCK_N - 1) / BLOCK_N;
-  int n_t[Q_TILES];
-#pragma unroll
-  for (int t = 0; t < Q_TILES; ++t) {
-    const int r0 = pair * (Q_TILES * BLOCK_M) + t * BLOCK_M;
-    int n = 0;
-    if (r0 < p.Nq) {
-      if (p.causal) {
-        // bottom-right alignment: row i sees keys j <= i + (Nk - Nq)
-        const int last_key = min(r0 + BLOCK_M - 1, p.Nq - 1) + (p.Nk - p.Nq);
-        n = last_key < 0 ? 0 : min(nkv_total, last_key / BLOCK_N + 1);
-      } else {
-        n = nkv_total;
-      }
-    }
-    n_t[t] = n;
-  }
-  int* kv_keep_slot = reinterpret_cast<int*>(smem + C::MISC_OFF + 8);
-  if (p.keep != nullptr && p.msq == 0 && warp == PREFILL_SOFTMAX_WARPS + 3) {
-    // One key mask for every row of this head: tiles after the last one with
-    // any key kept are skipped by every role.
+  if (trim && warp == PREFILL_SOFTMAX_WARPS + 3) {
+    const int bh = cta % (p.B * p.H);
     const int b = bh / p.H, h = bh % p.H;
     const uint32_t* kb = p.keep + b * p.msb + h * p.msh;
     const int nwords = (p.Nk + 31) >> 5;
@@ -242,16 +291,18 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   }
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < NK; ++i) mbar_init(full_k + i, 1);
-    for (int i = 0; i < NV; ++i) mbar_init(full_v + i, 1);
-    for (int i = 0; i < NR; ++i) mbar_init(rel + i, Q_TILES);  // both MMA-issuing warps
     for (int t = 0; t < Q_TILES; ++t) {
+      mbar_init(q_full + t, 1);
+      mbar_init(q_free + t, 1);
       mbar_init(s_full + t, 1);
       mbar_init(p_full + t, 128);
       mbar_init(o_done + t, 1);
       mbar_init(s_free + t, 128);
     }
+    for (int i = 0; i < NK; ++i) mbar_init(full_k + i, 1);
+    for (int i = 0; i < NV; ++i) mbar_init(full_v + i, 1);
+    for (int i = 0; i < NR; ++i) mbar_init(rel + i, Q_TILES);  // both MMA-issuing warps
+    mbar_init(unit_done, Q_TILES);
     mbar_init(drain, Q_TILES);
     *abort_flag = 0;
     fence_mbar_init();
@@ -264,80 +315,102 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (p.keep != nullptr && p.msq == 0) {
-    const int kv_keep = *kv_keep_slot;
-#pragma unroll
-    for (int t = 0; t < Q_TILES; ++t) n_t[t] = min(n_t[t], kv_keep);
-  }
-  const int n_max = max(n_t[0], n_t[1]);
+  const int kv_keep = trim ? *kv_keep_slot : INT_MAX;
+  // Every role walks the same unit sequence; barrier phases run on across
+  // units (counts of units, key tiles and per-tile steps done so far).
+  auto unit_at = [&](int k) { return unit_of(cta, k, G, snake); };
 
   if (warp >= PREFILL_SOFTMAX_WARPS) {
-    setmaxnreg_dec<PREFILL_PRODUCER_REGS>();
+    setmaxnreg_dec<prefill_producer_regs(D)>();
+    const bool leader = lane == 0;
     if (warp == PREFILL_TMA_WARP) {
-      // ---------------------------------------------------------- TMA producer
+      // ------------------------------------------------------ K/V TMA producer
       // The whole warp runs the loop and waits; lane 0 issues the copies.
-      const bool leader = lane == 0;
+      // Key tile g (counted over all units of this CTA) goes to K slot g % NK
+      // once tile g - NK was released, and to V slot g % NV once tile g - NV
+      // was released (release of tile i is phase i / NR of rel[i % NR]).
       if (leader) {
-        tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmO);
-        const int rq = pair * (Q_TILES * BLOCK_M);
-        mbar_arrive_expect_tx(q_full, Q_TILES * C::TILE_BYTES);
-        for (int t = 0; t < Q_TILES; ++t)
-          for (int b = 0; b < C::NBOX; ++b)
-            tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full, 64 * b, rq + t * BLOCK_M, bh);
       }
-      // Tile jj goes to K slot jj % NK once tile jj - NK was released, and to
-      // V slot jj % NV once tile jj - NV was released (release of tile i is
-      // phase i / NR of rel[i % NR]).
       auto wait_rel = [&](int i) -> bool {
         if (i < 0) return true;
-        const bool w = mbar_wait(rel + (i % NR), static_cast<uint32_t>((i / NR) & 1), lim, p.status, abort_flag, FA_SUSPEND_NS);
+        const bool w = mbar_wait(rel + (i % NR), static_cast<uint32_t>((i / NR) & 1), lim, p.status, abort_flag);
         return __all_sync(0xffffffffu, w) != 0;
       };
-      int nlk = 0, nlv = 0;  // K / V tiles loaded so far
+      int g = 0, nlk = 0, nlv = 0;
       bool ok = true;
-      for (int jj = 0; ok && jj < n_max; ++jj) {
-        if (!(ok = wait_rel(jj - NK))) break;
-        if (leader) {
-          uint8_t* dst = sK + (jj % NK) * C::TILE_BYTES;
-          mbar_arrive_expect_tx(full_k + (jj % NK), C::TILE_BYTES);
-          for (int b = 0; b < C::NBOX; ++b)
-            tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full_k + (jj % NK), 64 * b, jj * BLOCK_N, bh);
+      for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= U) break;
+        const Unit w = unit_info(p, u, kv_keep);
+        const int n_max = max(w.n0, w.n1);
+        for (int jj = 0; jj < n_max; ++jj, ++g) {
+          if (!(ok = wait_rel(g - NK))) break;
+          if (leader) {
+            uint8_t* dst = sK + (g % NK) * C::TILE_BYTES;
+            mbar_arrive_expect_tx(full_k + (g % NK), C::TILE_BYTES);
+            for (int b = 0; b < C::NBOX; ++b)
+              tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full_k + (g % NK), 64 * b, jj * BLOCK_N, w.bh);
+          }
+          ++nlk;
+          if (!(ok = wait_rel(g - NV))) break;
+          if (leader) {
+            uint8_t* dst = sV + (g % NV) * C::TILE_BYTES;
+            mbar_arrive_expect_tx(full_v + (g % NV), C::TILE_BYTES);
+            for (int b = 0; b < C::NBOX; ++b)
+              tma_load_3d(dst + b * C::BOX_BYTES, &tmV, full_v + (g % NV), 64 * b, jj * BLOCK_N, w.bh);
+          }
+          ++nlv;
         }
-        ++nlk;
-        if (!(ok = wait_rel(jj - NV))) break;
-        if (leader) {
-          uint8_t* dst = sV + (jj % NV) * C::TILE_BYTES;
-          mbar_arrive_expect_tx(full_v + (jj % NV), C::TILE_BYTES);
-          for (int b = 0; b < C::NBOX; ++b)
-            tma_load_3d(dst + b * C::BOX_BYTES, &tmV, full_v + (jj % NV), 64 * b, jj * BLOCK_N, bh);
-        }
-        ++nlv;
       }
       if (!ok && leader) {
         // error path: let the copies already issued land before the CTA exits
-        mbar_wait_drain(q_full, 0, lim);
         for (int n = max(0, nlk - NK); n < nlk; ++n) mbar_wait_drain(full_k + (n % NK), (n / NK) & 1, lim);
         for (int n = max(0, nlv - NV); n < nlv; ++n) mbar_wait_drain(full_v + (n % NV), (n / NV) & 1, lim);
       }
       __syncwarp();
+    } else if (warp == PREFILL_SOFTMAX_WARPS + 3) {
+      // ------------------------------------------------------- Q TMA producer
+      // Q_t of unit k goes into its buffer once unit k-1 is done with it
+      // (q_free_t, phase k-1).
+      if (leader) tma_prefetch_desc(&tmQ);
+      int issued[Q_TILES] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= U) break;
+        const Unit w = unit_info(p, u, kv_keep);
+        for (int t = 0; t < Q_TILES && ok; ++t) {
+          if (k > 0) {
+            ok = mbar_wait(q_free + t, (k - 1) & 1, lim, p.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+          }
+          if (leader) {
+            mbar_arrive_expect_tx(q_full + t, C::TILE_BYTES);
+            for (int b = 0; b < C::NBOX; ++b)
+              tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full + t, 64 * b,
+                          w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh);
+          }
+          ++issued[t];
+        }
+      }
+      if (!ok && leader) {
+        for (int t = 0; t < Q_TILES; ++t)
+          if (issued[t] > 0) mbar_wait_drain(q_full + t, (issued[t] - 1) & 1, lim);
+      }
+      __syncwarp();
     } else if (warp == PREFILL_MMA_WARP0 || warp == PREFILL_MMA_WARP0 + 1) {
       // ---------------------------------------------------------- MMA issuers
-      // One warp per Q tile (tile 0 first). tcgen05.mma
-      // issue only runs about one instruction ahead of the tensor pipe, so
-      // every barrier wait or commit of a lone issuing warp would leave the
-      // pipe idle; with two issuers each one's waits overlap the other's MMAs.
-      // The whole warp runs the loop and waits; lane 0 issues MMAs and commits.
+      // One warp per Q tile (tile 0 first). tcgen05.mma issue only runs about
+      // one instruction ahead of the tensor pipe, so every barrier wait or
+      // commit of a lone issuing warp would leave the pipe idle; with two
+      // issuers each one's waits overlap the other's MMAs. The whole warp runs
+      // the loop and waits; lane 0 issues MMAs and commits.
       const int t = warp - PREFILL_MMA_WARP0;
-      const bool leader = lane == 0;
-      bool ok = mbar_wait(q_full, 0, lim, p.status, abort_flag, FA_SUSPEND_NS);
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
       const uint32_t sQa = smem_u32(sQ) + t * C::TILE_BYTES;
-      const uint32_t sKa = smem_u32(sK);
-      const uint32_t sVa = smem_u32(sV);
       // Low descriptor words of Q_t, K slot 0 and V slot 0 (every operand
       // shares the high word: 1024-byte 8-row groups, 128-byte swizzle). The
       // K-step kk of Q and K (K-major) starts (kk / 4) boxes plus (kk % 4) x 32
@@ -345,325 +418,395 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       // 2048 bytes in. Another ring slot adds its offset to the low word.
       constexpr uint32_t DHI = sdesc_sw128_hi(1024);
       const uint32_t q_lo = sdesc_sw128_lo(sQa, 16);
-      const uint32_t k_lo = sdesc_sw128_lo(sKa, 16);
-      const uint32_t v_lo = sdesc_sw128_lo(sVa, C::BOX_BYTES);
-      const int nt = n_t[t];
+      const uint32_t k_lo = sdesc_sw128_lo(smem_u32(sK), 16);
+      const uint32_t v_lo = sdesc_sw128_lo(smem_u32(sV), C::BOX_BYTES);
       const uint32_t dS = tmem + BLOCK_N * t;
       const uint32_t dO = tmem + C::O_COL + D * t;
       const uint32_t aP = tmem + C::P_COL + C::P_STRIDE * t;
+      bool ok = true;
+      bool issued_any = false;
 
       auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
-        ok = mbar_wait(bar, parity, lim, p.status, abort_flag, FA_SUSPEND_NS);
+        ok = mbar_wait(bar, parity, lim, p.status, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         return ok;
       };
-      auto wait_bar2 = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t* c = nullptr,
+      // waits for up to three (barrier, parity) pairs; null barriers are skipped
+      auto wait_bars = [&](uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, uint64_t* c = nullptr,
                            uint32_t pc = 0) {
-        ok = mbar_wait2(a, pa, b, pb, lim, p.status, abort_flag, FA_SUSPEND_NS, c, pc);
+        if (a == nullptr) {
+          a = b;
+          pa = pb;
+        }
+        if (b == nullptr) {
+          b = a;
+          pb = pa;
+        }
+        ok = (a == nullptr) || mbar_wait2(a, pa, b, pb, lim, p.status, abort_flag, c, pc);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         return ok;
       };
-      auto fk_bar = [&](int jj) { return full_k + (jj % NK); };
-      auto fk_par = [&](int jj) { return static_cast<uint32_t>((jj / NK) & 1); };
-      auto fv_bar = [&](int jj) { return full_v + (jj % NV); };
-      auto fv_par = [&](int jj) { return static_cast<uint32_t>((jj / NV) & 1); };
-      auto issue_s = [&](int jj) {  // S_t = Q_t K_jj^T
-        if (leader) {
-          const uint32_t kb = k_lo + static_cast<uint32_t>(((jj % NK) * C::TILE_BYTES) >> 4);
+
+      int g0 = 0;          // key tiles of earlier units (ring position)
+      int c0 = 0, c1 = 0;  // steps of tile 0 / tile 1 in earlier units
+      for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= U) break;
+        const Unit w = unit_info(p, u, kv_keep);
+        const int nt = t ? w.n1 : w.n0;
+        const int ct = t ? c1 : c0;  // this tile's step count before the unit
+        const int n_max = max(w.n0, w.n1);
+        // Both issuers finish unit k-1 before either starts unit k: every
+        // barrier phase of unit k-1 is then complete or being waited for in
+        // order, which keeps the parity waits below unambiguous.
+        if (k > 0 && !wait_bar(unit_done, (k - 1) & 1)) break;
+        if (nt > 0 && !wait_bar(q_full + t, k & 1)) break;
+
+        auto fk_bar = [&](int jj) { return full_k + ((g0 + jj) % NK); };
+        auto fk_par = [&](int jj) { return static_cast<uint32_t>(((g0 + jj) / NK) & 1); };
+        auto fv_bar = [&](int jj) { return full_v + ((g0 + jj) % NV); };
+        auto fv_par = [&](int jj) { return static_cast<uint32_t>(((g0 + jj) / NV) & 1); };
+        auto issue_s = [&](int jj) {  // S_t = Q_t K_jj^T
+          if (lane == 0) {
+            const uint32_t kb = k_lo + static_cast<uint32_t>((((g0 + jj) % NK) * C::TILE_BYTES) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-            mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, C::IDESC_S, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+              mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, C::IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(s_full + t);
+            // the unit's last score MMA: Q_t is free once it (and all before it) completed
+            if (C::O_STAGE && jj == nt - 1) mma_commit(q_free + t);
           }
-          mma_commit(s_full + t);
-        }
-      };
-      auto issue_pv = [&](int jj) {  // O_t (+)= P_t V_jj
-        if (leader) {
-          const uint32_t vb = v_lo + static_cast<uint32_t>(((jj % NV) * C::TILE_BYTES) >> 4);
+          issued_any = true;
+        };
+        auto issue_pv = [&](int jj) {  // O_t (+)= P_t V_jj
+          if (lane == 0) {
+            const uint32_t vb = v_lo + static_cast<uint32_t>((((g0 + jj) % NV) * C::TILE_BYTES) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-            mma_ts_w(dO, aP + kk * 8, vb + kk * (2048 >> 4), DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(o_done + t);
-        }
-      };
-      // Key tile jj is released by both issuers (rel counts 2): by a commit
-      // when this warp's MMAs read it, by a plain arrive when they did not (a
-      // tile past this Q tile's range). A commit from a thread with no tcgen05
-      // operation to track is not relied on to arrive. An unused tile is first
-      // waited for (both loads landed), so the arrive lands in that tile's
-      // phase: an idle warp must not run around the ring ahead of the loads.
-      auto release = [&](int jj, bool used) {
-        if (!used && !wait_bar2(fk_bar(jj), fk_par(jj), fv_bar(jj), fv_par(jj))) return;
-        if (leader) {
-          if (used) mma_commit(rel + (jj % NR));
-          else mbar_arrive(rel + (jj % NR));
-        }
-      };
+            for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+              mma_ts_w(dO, aP + kk * 8, vb + kk * (2048 >> 4), DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(o_done + t);
+          }
+        };
+        // Key tile jj is released by both issuers (rel counts 2): by a commit
+        // when this warp's MMAs read it, by a plain arrive when they did not (a
+        // tile past this Q tile's range). A commit from a thread with no
+        // tcgen05 operation to track is not relied on to arrive. An unused tile
+        // is first waited for (both loads landed), so the arrive lands in that
+        // tile's phase: an idle warp must not run around the ring ahead of the
+        // loads.
+        auto release = [&](int jj, bool used) {
+          if (!used && !wait_bars(fk_bar(jj), fk_par(jj), fv_bar(jj), fv_par(jj))) return;
+          if (lane == 0) {
+            if (used) mma_commit(rel + ((g0 + jj) % NR));
+            else mbar_arrive(rel + ((g0 + jj) % NR));
+          }
+        };
+        // The two tiles' score MMAs alternate: S_{0,j} is issued only after
+        // S_{1,j-1} has completed and S_{1,j} only after S_{0,j} has completed
+        // (while both tiles still have key tiles). Without this order nothing
+        // keeps the tiles half a period apart, and they drift into lockstep:
+        // both score MMAs share the tensor pipe at once and then both softmax
+        // warpgroups share the SM's exponential units at once. The chain of
+        // waits also keeps each parity wait on the other tile's s_full
+        // unambiguous (that barrier is at most one phase behind or ahead).
+        auto order_bar = [&](int jj) -> uint64_t* {
+          if (!FA_SORDER) return nullptr;
+          if (t == 0) return (jj >= 1 && jj - 1 < w.n1) ? s_full + 1 : nullptr;
+          return (jj < w.n0) ? s_full + 0 : nullptr;
+        };
+        auto order_par = [&](int jj) -> uint32_t {
+          return static_cast<uint32_t>((t == 0 ? c1 + jj - 1 : c0 + jj) & 1);
+        };
+        // (The first PV of a unit overwrites O_t, which the previous unit's
+        // epilogue read: that is implied by p_full of the unit's first step,
+        // which the softmax arrives on only after that epilogue.)
 
-      // The two tiles' score MMAs alternate: S_{0,j} is issued only after
-      // S_{1,j-1} has completed and S_{1,j} only after S_{0,j} has completed
-      // (while both tiles still have key tiles). Without this order nothing
-      // keeps the tiles half a period apart, and they drift into lockstep:
-      // both score MMAs share the tensor pipe at once and then both softmax
-      // warpgroups share the SM's exponential units at once. The chain of
-      // waits also keeps each parity wait on the other tile's s_full
-      // unambiguous (that barrier is at most one phase behind or ahead).
-      // (barrier, parity) that S_{t,jj} must wait for, or null
-      auto order_bar = [&](int jj) -> uint64_t* {
-        if (!FA_SORDER) return nullptr;
-        if (t == 0) return (jj >= 1 && jj - 1 < n_t[1]) ? s_full + 1 : nullptr;
-        return (jj < n_t[0]) ? s_full + 0 : nullptr;
-      };
-      auto order_par = [&](int jj) -> uint32_t { return static_cast<uint32_t>((t == 0 ? jj - 1 : jj) & 1); };
+        // Ping-pong: the second Q tile starts once the first tile's first
+        // softmax is done, so one tile's exponentials overlap the other tile's
+        // MMAs instead of both tiles competing for the same unit at once.
+        if (C::STAGGER && t == 1 && w.n0 >= FA_STAGGER_MIN_TILES && nt > 0 && !wait_bar(p_full + 0, c0 & 1)) break;
 
-      // Ping-pong: the second Q tile starts once the first tile's first
-      // softmax is done, so one tile's exponentials overlap the other tile's
-      // MMAs instead of both tiles competing for the same unit at once.
-      if (C::STAGGER && t == 1 && n_t[0] >= FA_STAGGER_MIN_TILES && nt > 0) wait_bar(p_full + 0, 0);
-
-      if (C::SEP_P) {
-        // Software pipeline: S_{j+1} is issued as soon as the softmax has read
-        // S_j (s_free), so the next scores are computed while it exponentiates.
-        if (ok && nt > 0 && wait_bar2(fk_bar(0), fk_par(0), fk_bar(0), fk_par(0), order_bar(0), order_par(0)))
-          issue_s(0);
-        for (int jj = 0; ok && jj < n_max; ++jj) {
-          if (jj + 1 < nt) {
-            if (!wait_bar2(fk_bar(jj + 1), fk_par(jj + 1), s_free + t, jj & 1, order_bar(jj + 1), order_par(jj + 1)))
+        if (C::SEP_P) {
+          // Software pipeline: S_{j+1} is issued as soon as the softmax has
+          // read S_j (s_free), so the next scores are computed while it
+          // exponentiates. The first S of a unit needs the last S of the
+          // previous one read.
+          if (nt > 0) {
+            if (!wait_bars(fk_bar(0), fk_par(0), ct > 0 ? s_free + t : nullptr,
+                           static_cast<uint32_t>((ct - 1) & 1), order_bar(0), order_par(0)))
               break;
-            issue_s(jj + 1);
+            issue_s(0);
           }
-          if (jj < nt) {
-            if (!wait_bar2(p_full + t, jj & 1, fv_bar(jj), fv_par(jj))) break;
-            issue_pv(jj);
+          for (int jj = 0; ok && jj < n_max; ++jj) {
+            if (jj + 1 < nt) {
+              if (!wait_bars(fk_bar(jj + 1), fk_par(jj + 1), s_free + t, static_cast<uint32_t>((ct + jj) & 1),
+                             order_bar(jj + 1), order_par(jj + 1)))
+                break;
+              issue_s(jj + 1);
+            }
+            if (jj < nt) {
+              if (!wait_bars(p_full + t, static_cast<uint32_t>((ct + jj) & 1), fv_bar(jj), fv_par(jj))) break;
+              issue_pv(jj);
+            }
+            release(jj, jj < nt);
           }
-          release(jj, jj < nt);
+        } else {
+          // P aliases S in TMEM: S_{t,j} may only be written after PV_{t,j-1}
+          // (which reads P_{t,j-1} from the same columns) has completed; across
+          // units that is the previous unit's last PV.
+          for (int jj = 0; ok && jj < n_max; ++jj) {
+            if (jj < nt) {
+              if (!wait_bars(fk_bar(jj), fk_par(jj), (ct + jj > 0) ? o_done + t : nullptr,
+                             static_cast<uint32_t>((ct + jj - 1) & 1), order_bar(jj), order_par(jj)))
+                break;
+              issue_s(jj);
+              if (!wait_bars(p_full + t, static_cast<uint32_t>((ct + jj) & 1), fv_bar(jj), fv_par(jj))) break;
+              issue_pv(jj);
+            }
+            release(jj, jj < nt);
+          }
         }
-      } else {
-        // P aliases S in TMEM: S_{t,j} may only be written after PV_{t,j-1}
-        // (which reads P_{t,j-1} from the same columns) has completed.
-        for (int jj = 0; ok && jj < n_max; ++jj) {
-          if (jj < nt) {
-            const bool w = (jj > 0) ? wait_bar2(fk_bar(jj), fk_par(jj), o_done + t, (jj - 1) & 1, order_bar(jj),
-                                                order_par(jj))
-                                    : wait_bar2(fk_bar(jj), fk_par(jj), fk_bar(jj), fk_par(jj), order_bar(jj),
-                                                order_par(jj));
-            if (!w) break;
-            issue_s(jj);
-            if (!wait_bar2(p_full + t, jj & 1, fv_bar(jj), fv_par(jj))) break;
-            issue_pv(jj);
-          }
-          release(jj, jj < nt);
+        if (!ok) break;
+        if (lane == 0) {
+          if (C::O_STAGE && nt == 0) mbar_arrive(q_free + t);
+          mbar_arrive(unit_done);
         }
+        g0 += n_max;
+        c0 += w.n0;
+        c1 += w.n1;
       }
       // every MMA both issuers issued must finish before TMEM is released
-      if (leader) {
-        if (nt > 0) mma_commit(drain);
+      if (lane == 0) {
+        if (issued_any) mma_commit(drain);
         else mbar_arrive(drain);
         mbar_wait_drain(drain, 0, lim);
       }
       __syncwarp();
     }
   } else {
-    setmaxnreg_inc<PREFILL_SOFTMAX_REGS>();
+    setmaxnreg_inc<prefill_softmax_regs(D)>();
     // ------------------------------------------------- softmax / correction
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const int r0 = pair * (Q_TILES * BLOCK_M) + t * BLOCK_M;
-    const int qi = r0 + row;
-    const int n = n_t[t];
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + BLOCK_N * t;
     const uint32_t tO = tmem + lane_base + C::O_COL + D * t;
     const uint32_t tP = tmem + lane_base + C::P_COL + C::P_STRIDE * t;
     const float sl2 = p.scale_log2;
-    const int delta = p.Nk - p.Nq;
-    const int diag = qi + delta;          // last key this row may see (causal)
-    const int tile_lim = r0 + delta;      // last key the first row of the tile may see
-    const int nwords = (p.Nk + 31) >> 5;
-    const uint32_t* krow = nullptr;
-    if (p.keep != nullptr && qi < p.Nq) {
-      const int b = bh / p.H, h = bh % p.H;
-      krow = p.keep + b * p.msb + h * p.msh + static_cast<int64_t>(qi) * p.msq;
-    }
-    float m = -INFINITY;  // running max (possibly stale, see below), log2 units of the scaled score
-    float l = 0.f;        // running sum of exponentials on the base m
-    bool ok = true;
     const uint64_t sl2x2 = f2pack(sl2, sl2);
+    const int delta = p.Nk - p.Nq;
+    const int nwords = (p.Nk + 31) >> 5;
+    uint8_t* sO = (C::O_STAGE ? smem + C::O_OFF : sQ) + t * C::TILE_BYTES;
+    const bool storer = wq == 0 && lane == 0;
+    bool ok = true;
+    int ct = 0;  // this tile's steps in earlier units
 
-    // Barrier polls are issued early and their results used late (a poll on a
-    // completed barrier still costs a shared-memory round trip, long while the
-    // tensor core streams operands from shared memory): s_full of the next key
-    // tile right after P is stored, o_done of the previous PV halfway through
-    // the exponentials. A poll that finds the phase incomplete falls back to
-    // the bounded wait.
-    uint32_t s_ready = 0;
-    for (int j = 0; j < n; ++j) {
-      if (!__all_sync(0xffffffffu, s_ready)) {
-        ok = mbar_wait(s_full + t, j & 1, lim, p.status, abort_flag, FA_SUSPEND_NS);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+    // Every thread of the tile walks every unit and reaches the epilogue's
+    // named barrier once per unit, on the error path too (work is skipped,
+    // barriers are not).
+    for (int k = 0;; ++k) {
+      const int u = unit_at(k);
+      if (u >= U) break;
+      const Unit w = unit_info(p, u, kv_keep);
+      const int bh = w.bh;
+      const int n = t ? w.n1 : w.n0;
+      const int r0 = w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M;
+      const int qi = r0 + row;
+      const int diag = qi + delta;      // last key this row may see (causal)
+      const int tile_lim = r0 + delta;  // last key the first row of the tile may see
+      const uint32_t* krow = nullptr;
+      if (p.keep != nullptr && qi < p.Nq) {
+        const int b = bh / p.H, h = bh % p.H;
+        krow = p.keep + b * p.msb + h * p.msh + static_cast<int64_t>(qi) * p.msq;
       }
-      tc_fence_after();
-      uint32_t s[BLOCK_N];
-      tmem_ld32(tS + 0, s);
-      tmem_ld32(tS + 32, s + 32);
-      tmem_ld32(tS + 64, s + 64);
-      tmem_ld32(tS + 96, s + 96);
-      tmem_ld_wait32(s);
-      reg_fence32(s + 32);
-      reg_fence32(s + 64);
-      reg_fence32(s + 96);
-      if (C::SEP_P) {  // S_t may be overwritten with the next tile's scores
-        tc_fence_before();
-        mbar_arrive(s_free + t);
-      }
+      float m = -INFINITY;  // running max (possibly stale, see below), log2 units of the scaled score
+      float l = 0.f;        // running sum of exponentials on the base m
 
-      const int kbase = j * BLOCK_N;
-      uint32_t kw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      bool keep_all = true;
-      if (krow != nullptr) {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int wi = (kbase >> 5) + w;
-          kw[w] = wi < nwords ? __ldg(krow + wi) : 0u;
-        }
-        keep_all = (kw[0] & kw[1] & kw[2] & kw[3]) == 0xffffffffu;
-      }
-      // tiles whose 128 keys are all kept for every row of the warp skip the
-      // element-wise mask (warp-uniform choice of code path)
-      const bool need_mask = (kbase + BLOCK_N > p.Nk) || (p.causal && kbase + BLOCK_N - 1 > tile_lim) ||
-                             !__all_sync(0xffffffffu, keep_all);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < BLOCK_N; ++c) {
-          const int key = kbase + c;
-          bool vis = key < p.Nk;
-          if (p.causal) vis = vis && key <= diag;
-          vis = vis && ((kw[c >> 5] >> (c & 31)) & 1u);
-          if (!vis) s[c] = f2u(-INFINITY);
-        }
-      }
-      // row max: 8 independent chains of three-input maxima, then a short tree
-      float mxa[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        float v = u2f(s[a * 16]);
-#pragma unroll
-        for (int e = 1; e + 1 < 16; e += 2) v = fmax3(v, u2f(s[a * 16 + e]), u2f(s[a * 16 + e + 1]));
-        mxa[a] = fmaxf(v, u2f(s[a * 16 + 15]));
-      }
-      const float mx = fmaxf(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(fmax3(mxa[3], mxa[4], mxa[5]), mxa[6], mxa[7]));
-      const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * sl2;
-      // Lazy rescale: keep the running base m unless this tile's max exceeds it
-      // by more than RESCALE_LOG2; exponentials are then at most 2^RESCALE_LOG2,
-      // and l and O share the same (stale) base, so o / l is unchanged.
-      const bool bump = m_tile > m + C::RESCALE_LOG2;
-      const float m_new = bump ? m_tile : m;
-      const float alpha = bump ? ex2_approx(m - m_new) : 1.f;  // 0 while nothing was accumulated
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const uint64_t nm2 = f2pack(-m_use, -m_use);
-      uint32_t pk[BLOCK_N / 2];
-      uint32_t o_ready = 0;
-      const uint32_t o_poll = (C::SEP_P && j > 0) ? smem_u32(o_done + t) : 0u;
-      const uint32_t o_par = static_cast<uint32_t>((j - 1) & 1);
-      // (with no FMA-pipe pairs both instantiations are the same code: keep
-      // one copy of the unrolled loop in the instruction cache)
-      const float rowsum = (C::EMU_PAIRS > 0 && need_mask)
-                               ? softmax_tile_p<true, C::EMU_PAIRS>(s, sl2x2, nm2, pk, o_poll, o_par, &o_ready)
-                               : softmax_tile_p<false, C::EMU_PAIRS>(s, sl2x2, nm2, pk, o_poll, o_par, &o_ready);
-      if (C::SEP_P && j > 0) {
-        // P_t and O_t are free once PV_{t,j-1} has completed; it ran while
-        // the exponentials above were computed
-        if (!__all_sync(0xffffffffu, o_ready)) {
-          ok = mbar_wait(o_done + t, (j - 1) & 1, lim, p.status, abort_flag, FA_SUSPEND_NS);
+      // Barrier polls are issued early and their results used late: s_full of
+      // the next key tile right after P is stored, o_done of the previous PV
+      // halfway through the exponentials. A poll that finds the phase
+      // incomplete falls back to the bounded wait.
+      uint32_t s_ready = 0;
+      for (int j = 0; ok && j < n; ++j) {
+        const uint32_t ph = static_cast<uint32_t>((ct + j) & 1);  // this step's phase parity
+        if (!__all_sync(0xffffffffu, s_ready)) {
+          ok = mbar_wait(s_full + t, ph, lim, p.status, abort_flag);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
         }
         tc_fence_after();
+        uint32_t s[BLOCK_N];
+        tmem_ld32(tS + 0, s);
+        tmem_ld32(tS + 32, s + 32);
+        tmem_ld32(tS + 64, s + 64);
+        tmem_ld32(tS + 96, s + 96);
+        tmem_ld_wait32(s);
+        reg_fence32(s + 32);
+        reg_fence32(s + 64);
+        reg_fence32(s + 96);
+        if (C::SEP_P) {  // S_t may be overwritten with the next tile's scores
+          tc_fence_before();
+          mbar_arrive(s_free + t);
+        }
+
+        const int kbase = j * BLOCK_N;
+        uint32_t kw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        bool keep_all = true;
+        if (krow != nullptr) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int wi = (kbase >> 5) + q;
+            kw[q] = wi < nwords ? __ldg(krow + wi) : 0u;
+          }
+          keep_all = (kw[0] & kw[1] & kw[2] & kw[3]) == 0xffffffffu;
+        }
+        // tiles whose 128 keys are all kept for every row of the warp skip the
+        // element-wise mask (warp-uniform choice of code path)
+        const bool need_mask = (kbase + BLOCK_N > p.Nk) || (p.causal && kbase + BLOCK_N - 1 > tile_lim) ||
+                               !__all_sync(0xffffffffu, keep_all);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < BLOCK_N; ++c) {
+            const int key = kbase + c;
+            bool vis = key < p.Nk;
+            if (p.causal) vis = vis && key <= diag;
+            vis = vis && ((kw[c >> 5] >> (c & 31)) & 1u);
+            if (!vis) s[c] = f2u(-INFINITY);
+          }
+        }
+        // row max: 8 independent chains of three-input maxima, then a short tree
+        float mxa[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+          float v = u2f(s[a * 16]);
+#pragma unroll
+          for (int e = 1; e + 1 < 16; e += 2) v = fmax3(v, u2f(s[a * 16 + e]), u2f(s[a * 16 + e + 1]));
+          mxa[a] = fmaxf(v, u2f(s[a * 16 + 15]));
+        }
+        const float mx =
+            fmaxf(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(fmax3(mxa[3], mxa[4], mxa[5]), mxa[6], mxa[7]));
+        const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+        // Lazy rescale: keep the running base m unless this tile's max exceeds it
+        // by more than RESCALE_LOG2; exponentials are then at most 2^RESCALE_LOG2,
+        // and l and O share the same (stale) base, so o / l is unchanged.
+        const bool bump = m_tile > m + C::RESCALE_LOG2;
+        const float m_new = bump ? m_tile : m;
+        const float alpha = bump ? ex2_approx(m - m_new) : 1.f;  // 0 while nothing was accumulated
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const uint64_t nm2 = f2pack(-m_use, -m_use);
+        uint32_t pk[BLOCK_N / 2];
+        uint32_t o_ready = 0;
+        const uint32_t o_poll = (C::SEP_P && j > 0) ? smem_u32(o_done + t) : 0u;
+        const uint32_t o_par = ph ^ 1u;  // the previous step's phase
+        // (with no FMA-pipe pairs both instantiations are the same code: keep
+        // one copy of the unrolled loop in the instruction cache)
+        const float rowsum = (C::EMU_PAIRS > 0 && need_mask)
+                                 ? softmax_tile_p<true, C::EMU_PAIRS>(s, sl2x2, nm2, pk, o_poll, o_par, &o_ready)
+                                 : softmax_tile_p<false, C::EMU_PAIRS>(s, sl2x2, nm2, pk, o_poll, o_par, &o_ready);
+        if (C::SEP_P && j > 0) {
+          // P_t and O_t are free once PV_{t,j-1} has completed; it ran while
+          // the exponentials above were computed. (At a unit's first step the
+          // previous unit's epilogue already waited for its last PV.)
+          if (!__all_sync(0xffffffffu, o_ready)) {
+            ok = mbar_wait(o_done + t, o_par, lim, p.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(tP, pk);
+        tmem_st32(tP + 32, pk + 32);
+        s_ready = (FA_EARLY_POLL && j + 1 < n) ? mbar_test(smem_u32(s_full + t), ph ^ 1u) : 0u;
+        l = fmaf(l, alpha, rowsum);
+        // O_t is quiescent here: PV_{t,j-1} has completed (waited above, or before
+        // S_{t,j} was issued) and PV_{t,j} waits for p_full.
+        if (j > 0 && __any_sync(0xffffffffu, bump)) {
+          const uint64_t al2 = f2pack(alpha, alpha);
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(tO + ch * 32, o);
+            tmem_ld_wait32(o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float y0, y1;
+              f2unpack(fmul2(f2pack(u2f(o[2 * i]), u2f(o[2 * i + 1])), al2), y0, y1);
+              o[2 * i] = f2u(y0);
+              o[2 * i + 1] = f2u(y1);
+            }
+            tmem_st32(tO + ch * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + t);
+        m = m_new;
       }
-      tmem_st32(tP, pk);
-      tmem_st32(tP + 32, pk + 32);
-      s_ready = (FA_EARLY_POLL && j + 1 < n) ? mbar_test(smem_u32(s_full + t), (j + 1) & 1) : 0u;
-      l = fmaf(l, alpha, rowsum);
-      // O_t is quiescent here: PV_{t,j-1} has completed (waited above, or before
-      // S_{t,j} was issued) and PV_{t,j} waits for p_full.
-      if (j > 0 && __any_sync(0xffffffffu, bump)) {
-        const uint64_t al2 = f2pack(alpha, alpha);
+
+      // ---- epilogue: O = o / l (0 for an empty row), lse = m + ln l (-inf for an empty row)
+      // O goes through shared memory into one TMA store per 64-column box. The
+      // staging buffer is this tile's Q tile: every S MMA that read it has
+      // completed once the last PV has (the issuer's commit covers all its
+      // earlier MMAs); a tile with no key tile ran no MMA, so there the Q load
+      // itself is waited for. Rows are written in the 128-byte-swizzled layout
+      // the tensor map expects; rows past Nq are clipped by the store. Once the
+      // store has read the buffer (q_free) the next Q may be loaded into it.
+      if (ok && (n > 0 || !C::O_STAGE)) {
+        ok = (n > 0) ? mbar_wait(o_done + t, static_cast<uint32_t>((ct + n - 1) & 1), lim, p.status, abort_flag)
+                     : mbar_wait(q_full + t, k & 1, lim, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+      }
+      // a separate staging buffer is rewritten only after the previous unit's
+      // store has read it (the storer waited for that before this barrier)
+      if (C::O_STAGE && k > 0) named_bar_sync(1 + t, 128);
+      if (ok) {
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const uint32_t srow = smem_u32(sO) + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
-          tmem_ld32(tO + ch * 32, o);
-          tmem_ld_wait32(o);
+          if (n > 0) {
+            tmem_ld32(tO + ch * 32, o);
+            tmem_ld_wait32(o);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float y0, y1;
-            f2unpack(fmul2(f2pack(u2f(o[2 * i]), u2f(o[2 * i + 1])), al2), y0, y1);
-            o[2 * i] = f2u(y0);
-            o[2 * i + 1] = f2u(y1);
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
           }
-          tmem_st32(tO + ch * 32, o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int c = ch * 4 + v;  // 16-byte chunk of the row: box c / 8, chunk c % 8 of the box
+            const uint32_t a = srow + static_cast<uint32_t>((c >> 3) * C::BOX_BYTES) +
+                               (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4);
+            st_shared_v4(a, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
         }
+        if (p.lse != nullptr && qi < p.Nq)
+          p.lse[static_cast<size_t>(bh) * p.Nq + qi] =
+              (l > 0.f) ? (m + lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full + t);
-      m = m_new;
-    }
-
-    // ---- epilogue: O = o / l (0 for an empty row), lse = m + ln l (-inf for an empty row)
-    // O goes through shared memory into one TMA store per 64-column box. The
-    // staging buffer is this tile's Q tile: every S MMA that read it has
-    // completed once the last PV has (the issuer's commit covers all its
-    // earlier MMAs); a tile with no key tile ran no MMA, so there the Q load
-    // itself is waited for. Rows are written in the 128-byte-swizzled layout
-    // the tensor map expects; rows past Nq are clipped by the store.
-    if (ok) {
-      ok = (n > 0) ? mbar_wait(o_done + t, (n - 1) & 1, lim, p.status, abort_flag, FA_SUSPEND_NS)
-                   : mbar_wait(q_full, 0, lim, p.status, abort_flag, FA_SUSPEND_NS);
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-    }
-    uint8_t* sO = sQ + t * C::TILE_BYTES;
-    if (ok) {
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      const uint32_t srow = smem_u32(sO) + static_cast<uint32_t>(row) * 128u;
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, 128);  // every thread of the tile, every unit, on every path
+      if (storer && *abort_flag == 0) {
+        if (r0 < p.Nq) {
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        if (n > 0) {
-          tmem_ld32(tO + ch * 32, o);
-          tmem_ld_wait32(o);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
+          for (int b = 0; b < C::NBOX; ++b) tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
+          bulk_commit_group();
+          bulk_wait_group_read_all();
         }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int c = ch * 4 + v;  // 16-byte chunk of the row: box c / 8, chunk c % 8 of the box
-          const uint32_t a = srow + static_cast<uint32_t>((c >> 3) * C::BOX_BYTES) +
-                             (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4);
-          st_shared_v4(a, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
+        if (!C::O_STAGE) mbar_arrive(q_free + t);
       }
-      if (p.lse != nullptr && qi < p.Nq)
-        p.lse[static_cast<size_t>(bh) * p.Nq + qi] =
-            (l > 0.f) ? (m + lg2_approx(l)) * 0.69314718055994530942f : -INFINITY;
+      ct += n;
     }
-    fence_proxy_async_smem();
-    named_bar_sync(1 + t, 128);  // every thread of the tile, on every path
-    if (wq == 0 && lane == 0 && r0 < p.Nq && *abort_flag == 0) {
-#pragma unroll
-      for (int b = 0; b < C::NBOX; ++b) tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
-      bulk_commit_group();
-      bulk_wait_group_all();
-    }
+    if (storer) bulk_wait_group_all();  // the last stores are complete before the CTA exits
   }
 
   tc_fence_before();
@@ -677,9 +820,16 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 template <int D>
 static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
+  // Persistent: one CTA per SM walks its share of the units, so the next
+  // unit's loads and first MMAs overlap the current one's epilogue. A key
+  // mask broadcast over rows (trimmed per unit) gets one CTA per unit, as does
+  // a head dimension where that measured faster.
   const long long units = static_cast<long long>(p.n_qpairs) * p.B * p.H;
-  fa_prefill_kernel<D><<<static_cast<unsigned>(units), PREFILL_THREADS, PrefillCfg<D>::SMEM, stream>>>(tq, tk, tv,
-                                                                                                      to, p);
+  const bool trim = p.keep != nullptr && p.msq == 0;
+  const long long ctas =
+      (trim || !PrefillCfg<D>::PERSIST) ? units : std::min<long long>(units, std::max(1, p.max_ctas));
+  fa_prefill_kernel<D><<<static_cast<unsigned>(ctas), PREFILL_THREADS, PrefillCfg<D>::SMEM, stream>>>(tq, tk, tv,
+                                                                                                     to, p);
   return cudaGetLastError();
 }
 

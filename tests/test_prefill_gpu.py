@@ -131,6 +131,30 @@ def test_key_padding_and_row_masks(fa, d):
         check_full(fa, q, k, v, 0.1, causal, keep, f"rowmask causal={causal}")
 
 
+# ------------------------------------------- several units per persistent CTA
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_units_per_cta(fa, d):
+    """B*H*ceil(Nq/256) well above the SM count, so every persistent CTA walks
+    several units with barrier phases running on across them. Nq = 300 leaves
+    the second Q tile of each head's last pair empty (rows from 384), and under
+    the causal mask the first tiles visit 1-3 key tiles, so units of different
+    lengths (and a first tile longer than the second) follow each other."""
+    q, k, v = W.make_qkv(4, 48, 300, 300, d, seed=21)
+    for causal in (False, True):
+        check_full(fa, q, k, v, 1 / math.sqrt(d), causal, None, f"many units d={d} causal={causal}")
+    keep = torch.rand(4, 48, 300, 300, generator=torch.Generator().manual_seed(4)) < 0.5
+    check_full(fa, q, k, v, 1 / math.sqrt(d), True, keep, f"many units row mask d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_units_rectangular(fa, d):
+    """Nq != Nk with several units per CTA: 480 units of 6 key tiles each
+    (non-causal), and bottom-right causal alignment with Nk > Nq."""
+    q, k, v = W.make_qkv(2, 80, 520, 700, d, seed=22)
+    for causal in (False, True):
+        check_full(fa, q, k, v, 1 / math.sqrt(d), causal, None, f"rect units d={d} causal={causal}")
+
+
 def test_scale_zero_is_uniform(fa):
     q, k, v = W.make_qkv(1, 1, 130, 140, 64, seed=6)
     check_full(fa, q, k, v, 0.0, False, None, "scale 0")
