@@ -31,6 +31,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -49,6 +51,19 @@ def measured_peaks():
         return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
                     bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def visible_pair_fraction(wp, causal: bool) -> float:
+    """Share of the nominal (query, key) pairs a workload's key padding leaves
+    visible (1.0 without padding); effective TFLOP/s = nominal x this share.
+    Causal visibility is bottom-right: row i sees keys j <= i + Nk - Nq."""
+    if not wp.pad_heads:
+        return 1.0
+    i = np.arange(wp.Nq, dtype=np.int64)
+    end = np.clip(i + 1 + (wp.Nk - wp.Nq), 0, wp.Nk) if causal else np.full(wp.Nq, wp.Nk, dtype=np.int64)
+    full = int(end.sum())
+    padded = int(np.minimum(end, wp.pad_from).sum())
+    return (wp.pad_heads * padded + (wp.H - wp.pad_heads) * full) / (wp.H * full)
 
 
 def kernel_hash(name: str) -> str:
@@ -418,6 +433,11 @@ def main():
             tag = "causal" if c else "noncausal"
             line["roofline"][f"ms_{tag}"] = tm / K * 1e3
             line["roofline"][f"tflops_{tag}"] = K * fm / tm / 1e12
+        if wp.pad_heads:
+            # key padding: the nominal FLOPs count the padded keys as well
+            share = sum(visible_pair_fraction(wp, c) * fm for c, fm in zip(modes, f_modes)) / f_p
+            line["roofline"]["visible_pair_share"] = share
+            line["roofline"]["tflops_effective"] = ach * share
     if do_d:
         ach = K * dec_bytes / t_d / 1e9
         line["decode"] = {"value": world * ach, "unit": "GB/s", "ms": t_d / K * 1e3, "bytes": dec_bytes,

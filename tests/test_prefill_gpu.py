@@ -202,6 +202,8 @@ def test_bounded_wait_reports_timeout_and_context_survives(fa):
 
 # ------------------------------------------------------- full-size workloads
 def _sampled(fa, w, causal, keep=None, full_heads=2, rows_per_head=256, seed=0):
+    """Every row of the first and last head (full_heads=2), plus rows_per_head
+    seeded rows (and the first and last row) of every head."""
     q, k, v = W.make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, seed=seed)
     o, lse = run(fa, q, k, v, w.scale, causal, keep)
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
@@ -228,20 +230,20 @@ def test_prefill_2k_d64(fa, causal):
 @pytest.mark.slow
 def test_prefill_8k_d128_causal(fa):
     w = W.WORKLOADS["prefill_8k"]
-    print(_sampled(fa, w, True, full_heads=2, rows_per_head=64))
+    print(_sampled(fa, w, True, full_heads=2, rows_per_head=1024))
 
 
 @pytest.mark.slow
 def test_prefill_32k_d128_causal(fa):
     w = W.WORKLOADS["prefill_32k"]
-    print(_sampled(fa, w, True, full_heads=0, rows_per_head=96))
+    print(_sampled(fa, w, True, full_heads=2, rows_per_head=1024))
 
 
 @pytest.mark.slow
 def test_prefill_32k_d128_causal_keypad(fa):
     w = W.WORKLOADS["prefill_32k_pad"]
     keep = W.key_padding_keep(w.B, w.H, w.Nk, w.pad_heads, w.pad_from)
-    print(_sampled(fa, w, True, keep=keep, full_heads=0, rows_per_head=96))
+    print(_sampled(fa, w, True, keep=keep, full_heads=2, rows_per_head=1024))
 
 
 def test_fma_pipe_exp2_error_bound(fa):
