@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -14,6 +15,10 @@
 
 #include "fa.h"
 #include "fa_common.cuh"
+
+#ifndef FA_TAIL_SPLIT
+#define FA_TAIL_SPLIT 1  // split a last, at most half-full round of Q-tile pairs into single tiles
+#endif
 
 namespace fa {
 // One status word per device; kernels atomicOr FA_DEV_* bits into it.
@@ -196,6 +201,19 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
   p.max_ctas = st->num_sms;
+  // Work units are Q-tile pairs. When the pairs leave a last round of CTAs
+  // (one per SM) at most half full, those last pairs are split into single
+  // Q tiles so that round ends sooner; not with a broadcast key mask, whose
+  // trimming assumes pair units.
+  {
+    const long long U = n_qpairs * BH;
+    const long long G = std::max(1, st->num_sms);
+    const long long r = U % G;
+    const bool trim = keep_bits != nullptr && mstride_q == 0;
+    const bool split = FA_TAIL_SPLIT && !trim && U >= G && r > 0 && 2 * r <= G;
+    p.split_from = static_cast<int>(split ? U - r : U);
+    p.units = static_cast<int>(split ? U + r : U);
+  }
   cudaError_t e = fa::launch_prefill(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   t_launches += 1;

@@ -62,6 +62,8 @@ struct PrefillParams {
   uint64_t wait_limit_ns;
   unsigned int* status;      // device status word
   int max_ctas;              // CTAs of a persistent launch (the SM count)
+  int units;                 // work units: Q-tile pairs, then single Q tiles (see split_from)
+  int split_from;            // units from here on are single tiles of the last pairs
 };
 
 struct DecodeParams {

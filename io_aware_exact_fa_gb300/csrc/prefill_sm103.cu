@@ -198,16 +198,24 @@ __device__ __forceinline__ bool mbar_wait2(uint64_t* a, uint32_t pa, uint64_t* b
   return true;
 }
 
-// Work unit u (0 <= u < BH * n_qpairs): Q-tile pair `pair` of head `bh`.
-// Causal runs the longest pairs first.
+// Work unit u: units below p.split_from are Q-tile pair u (pair `pair` of
+// head `bh`); the pairs from p.split_from on, which would fill only part of a
+// last round of CTAs, are split into two single-tile units each (tile 0, then
+// tile 1). Causal runs the longest pairs first.
 struct Unit {
   int bh, pair, n0, n1;  // n_t: key tiles Q tile t visits
+  bool act0, act1;       // whether this unit computes Q tile t at all
 };
 __device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u, int kv_keep) {
   const int BH = p.B * p.H;
   Unit w;
-  w.pair = p.causal ? (p.n_qpairs - 1 - u / BH) : (u / BH);
-  w.bh = u % BH;
+  int pu = u, only = -1;
+  if (u >= p.split_from) {
+    pu = p.split_from + (u - p.split_from) / 2;
+    only = (u - p.split_from) & 1;
+  }
+  w.pair = p.causal ? (p.n_qpairs - 1 - pu / BH) : (pu / BH);
+  w.bh = pu % BH;
   const int nkv_total = (p.Nk + BLOCK_N - 1) / BLOCK_N;
   int n[Q_TILES];
 #pragma unroll
@@ -223,10 +231,12 @@ __device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u, int kv_
         nt = nkv_total;
       }
     }
-    n[t] = min(nt, kv_keep);
+    n[t] = (only < 0 || only == t) ? min(nt, kv_keep) : 0;
   }
   w.n0 = n[0];
   w.n1 = n[1];
+  w.act0 = only != 1;
+  w.act1 = only != 0;
   return w;
 }
 // The k-th unit of CTA c of G, or a value >= U when it has no k-th unit.
@@ -268,7 +278,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
-  const int U = p.B * p.H * p.n_qpairs;
+  const int U = p.units;
   const int G = static_cast<int>(gridDim.x);
   const int cta = static_cast<int>(blockIdx.x);
   const bool snake = p.causal != 0;
@@ -389,10 +399,14 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
             if (!ok) break;
           }
           if (leader) {
-            mbar_arrive_expect_tx(q_full + t, C::TILE_BYTES);
-            for (int b = 0; b < C::NBOX; ++b)
-              tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full + t, 64 * b,
-                          w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh);
+            if (t ? w.act1 : w.act0) {
+              mbar_arrive_expect_tx(q_full + t, C::TILE_BYTES);
+              for (int b = 0; b < C::NBOX; ++b)
+                tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full + t, 64 * b,
+                            w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh);
+            } else {
+              mbar_arrive(q_full + t);  // a tile this unit does not compute: the phase completes empty
+            }
           }
           ++issued[t];
         }
@@ -615,6 +629,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       const Unit w = unit_info(p, u, kv_keep);
       const int bh = w.bh;
       const int n = t ? w.n1 : w.n0;
+      const bool active = t ? w.act1 : w.act0;  // else another unit computes these rows
       const int r0 = w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M;
       const int qi = r0 + row;
       const int diag = qi + delta;      // last key this row may see (causal)
@@ -756,7 +771,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       // itself is waited for. Rows are written in the 128-byte-swizzled layout
       // the tensor map expects; rows past Nq are clipped by the store. Once the
       // store has read the buffer (q_free) the next Q may be loaded into it.
-      if (ok && (n > 0 || !C::O_STAGE)) {
+      if (ok && active && (n > 0 || !C::O_STAGE)) {
         ok = (n > 0) ? mbar_wait(o_done + t, static_cast<uint32_t>((ct + n - 1) & 1), lim, p.status, abort_flag)
                      : mbar_wait(q_full + t, k & 1, lim, p.status, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
@@ -765,7 +780,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       // a separate staging buffer is rewritten only after the previous unit's
       // store has read it (the storer waited for that before this barrier)
       if (C::O_STAGE && k > 0) named_bar_sync(1 + t, 128);
-      if (ok) {
+      if (ok && active) {
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
         const uint32_t srow = smem_u32(sO) + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
@@ -796,7 +811,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       fence_proxy_async_smem();
       named_bar_sync(1 + t, 128);  // every thread of the tile, every unit, on every path
       if (storer && *abort_flag == 0) {
-        if (r0 < p.Nq) {
+        if (active && r0 < p.Nq) {
 #pragma unroll
           for (int b = 0; b < C::NBOX; ++b) tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
           bulk_commit_group();
@@ -824,7 +839,7 @@ static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk
   // unit's loads and first MMAs overlap the current one's epilogue. A key
   // mask broadcast over rows (trimmed per unit) gets one CTA per unit, as does
   // a head dimension where that measured faster.
-  const long long units = static_cast<long long>(p.n_qpairs) * p.B * p.H;
+  const long long units = p.units;
   const bool trim = p.keep != nullptr && p.msq == 0;
   const long long ctas =
       (trim || !PrefillCfg<D>::PERSIST) ? units : std::min<long long>(units, std::max(1, p.max_ctas));
