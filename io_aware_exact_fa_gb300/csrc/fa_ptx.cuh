@@ -10,6 +10,10 @@
 
 #include "fa_common.cuh"
 
+#ifndef FA_WAIT_SPIN
+#define FA_WAIT_SPIN 0  // poll with test_wait (never suspends) instead of try_wait
+#endif
+
 namespace fa {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -72,7 +76,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (FA_WAIT_SPIN ? mbar_test(a, parity) != 0u : mbar_try_wait(a, parity)) return true;
     if ((i & 31u) == 0u) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {

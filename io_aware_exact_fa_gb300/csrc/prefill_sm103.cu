@@ -67,6 +67,12 @@ namespace fa {
 #ifndef FA_PERSIST_D128
 #define FA_PERSIST_D128 0
 #endif
+#ifndef FA_UNIT_DONE_EARLY_D64
+#define FA_UNIT_DONE_EARLY_D64 0   // an issuer signals unit_done after its last S of a unit (else after its last PV)
+#endif
+#ifndef FA_UNIT_DONE_EARLY_D128
+#define FA_UNIT_DONE_EARLY_D128 1
+#endif
 #ifndef FA_O_STAGE
 #define FA_O_STAGE 1             // separate O staging buffers where shared memory allows (d = 64)
 #endif
@@ -122,6 +128,7 @@ struct PrefillCfg {
   // d = 128 the Q buffer also stages O, so the next Q waits for the epilogue
   // and one CTA per unit is faster.
   static constexpr bool PERSIST = (D == 64) ? FA_PERSIST_D64 : FA_PERSIST_D128;
+  static constexpr bool UNIT_DONE_EARLY = (D == 64) ? FA_UNIT_DONE_EARLY_D64 : FA_UNIT_DONE_EARLY_D128;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   uint64_t* p_full = s_full + Q_TILES;     // P_t of step c stored
   uint64_t* o_done = p_full + Q_TILES;     // PV_t of step c complete
   uint64_t* s_free = o_done + Q_TILES;     // S_t of step c read by the softmax
-  uint64_t* unit_done = s_free + Q_TILES;  // both issuers finished unit k (phase k)
+  uint64_t* unit_done = s_free + Q_TILES;  // both tiles' score MMAs of unit k completed (phase k)
   uint64_t* drain = unit_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
@@ -384,7 +391,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     } else if (warp == PREFILL_SOFTMAX_WARPS + 3) {
       // ------------------------------------------------------- Q TMA producer
       // Q_t of unit k goes into its buffer once unit k-1 is done with it
-      // (q_free_t, phase k-1).
+      // (q_free_t, phase k-1) and Q_t of unit k-1 has landed (q_full_t).
       if (leader) tma_prefetch_desc(&tmQ);
       int issued[Q_TILES] = {0, 0};
       bool ok = true;
@@ -394,7 +401,10 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         const Unit w = unit_info(p, u, kv_keep);
         for (int t = 0; t < Q_TILES && ok; ++t) {
           if (k > 0) {
-            ok = mbar_wait(q_free + t, (k - 1) & 1, lim, p.status, abort_flag);
+            // the buffer is free, and this warp's previous load into it has
+            // landed (nobody else waits for it when that tile had no key
+            // tile): a second expect_tx must not join an unfinished phase
+            ok = mbar_wait2(q_free + t, (k - 1) & 1, q_full + t, (k - 1) & 1, lim, p.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
           }
@@ -472,11 +482,19 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         const int nt = t ? w.n1 : w.n0;
         const int ct = t ? c1 : c0;  // this tile's step count before the unit
         const int n_max = max(w.n0, w.n1);
-        // Both issuers finish unit k-1 before either starts unit k: every
-        // barrier phase of unit k-1 is then complete or being waited for in
-        // order, which keeps the parity waits below unambiguous.
+        // Neither issuer starts unit k before both tiles' score MMAs of unit
+        // k-1 have completed (each issuer commits to unit_done after its last
+        // S of a unit, or arrives at the start when it has none): every phase
+        // of the other tile's s_full before this unit is then complete, which
+        // keeps the parity waits on it below unambiguous.
         if (k > 0 && !wait_bar(unit_done, (k - 1) & 1)) break;
-        if (nt > 0 && !wait_bar(q_full + t, k & 1)) break;
+        if (C::UNIT_DONE_EARLY && nt == 0 && lane == 0) mbar_arrive(unit_done);
+        // Q_t of unit k has landed (the Q producer has passed its wait for
+        // unit k-1). A tile without key tiles releases its Q buffer only after
+        // that: otherwise q_free_t could run two phases ahead of the Q
+        // producer's parity wait on it.
+        if (!wait_bar(q_full + t, k & 1)) break;
+        if (nt == 0 && C::O_STAGE && lane == 0) mbar_arrive(q_free + t);
 
         auto fk_bar = [&](int jj) { return full_k + ((g0 + jj) % NK); };
         auto fk_par = [&](int jj) { return static_cast<uint32_t>(((g0 + jj) / NK) & 1); };
@@ -491,8 +509,12 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
               mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, C::IDESC_S, kk > 0 ? 1u : 0u);
             }
             mma_commit(s_full + t);
-            // the unit's last score MMA: Q_t is free once it (and all before it) completed
-            if (C::O_STAGE && jj == nt - 1) mma_commit(q_free + t);
+            // the unit's last score MMA: Q_t is free once it (and all before it)
+            // completed, and the other issuer may start the next unit
+            if (jj == nt - 1) {
+              if (C::O_STAGE) mma_commit(q_free + t);
+              if (C::UNIT_DONE_EARLY) mma_commit(unit_done);
+            }
           }
           issued_any = true;
         };
@@ -585,10 +607,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          if (C::O_STAGE && nt == 0) mbar_arrive(q_free + t);
-          mbar_arrive(unit_done);
-        }
+        if (!C::UNIT_DONE_EARLY && lane == 0) mbar_arrive(unit_done);
         g0 += n_max;
         c0 += w.n0;
         c1 += w.n1;
