@@ -147,6 +147,23 @@ def test_many_units_per_cta(fa, d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_many_units_repeated(fa, d):
+    """Barrier phases that run on across units must stay in step on every run:
+    30 launches of a shape whose units alternate between two busy tiles and one
+    tile with no key tiles (B=4, H=48, Nq=Nk=300) must all finish without a
+    timed-out wait and give bit-identical outputs."""
+    q, k, v = W.make_qkv(4, 48, 300, 300, d, seed=23)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    for causal in (False, True):
+        ref = fa.fwd(dq, dk, dv, causal=causal)
+        for _ in range(30):
+            o, lse = fa.fwd(dq, dk, dv, causal=causal)
+            assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1])
+        torch.cuda.synchronize()
+        assert fa.device_status() == fa.FA_OK
+
+
+@pytest.mark.parametrize("d", [64, 128])
 def test_many_units_rectangular(fa, d):
     """Nq != Nk with several units per CTA: 480 units of 6 key tiles each
     (non-causal), and bottom-right causal alignment with Nk > Nq."""
