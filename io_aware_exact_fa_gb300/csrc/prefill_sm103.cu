@@ -73,6 +73,9 @@ namespace fa {
 #ifndef FA_UNIT_DONE_EARLY_D128
 #define FA_UNIT_DONE_EARLY_D128 1
 #endif
+#ifndef FA_LEAD_LONGER
+#define FA_LEAD_LONGER 1         // the Q tile with more key tiles issues its scores first
+#endif
 #ifndef FA_O_STAGE
 #define FA_O_STAGE 1             // separate O staging buffers where shared memory allows (d = 64)
 #endif
@@ -541,30 +544,37 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
             else mbar_arrive(rel + ((g0 + jj) % NR));
           }
         };
-        // The two tiles' score MMAs alternate: S_{0,j} is issued only after
-        // S_{1,j-1} has completed and S_{1,j} only after S_{0,j} has completed
-        // (while both tiles still have key tiles). Without this order nothing
-        // keeps the tiles half a period apart, and they drift into lockstep:
-        // both score MMAs share the tensor pipe at once and then both softmax
-        // warpgroups share the SM's exponential units at once. The chain of
-        // waits also keeps each parity wait on the other tile's s_full
-        // unambiguous (that barrier is at most one phase behind or ahead).
+        // The two tiles' score MMAs alternate: the leading tile's S_j is issued
+        // only after the other tile's S_{j-1} has completed, and the other
+        // tile's S_j only after the leader's S_j has completed (while both
+        // still have key tiles). Without this order nothing keeps the tiles
+        // half a period apart, and they drift into lockstep: both score MMAs
+        // share the tensor pipe at once and then both softmax warpgroups share
+        // the SM's exponential units at once. The chain of waits also keeps
+        // each parity wait on the other tile's s_full unambiguous (that barrier
+        // is at most one phase behind or ahead). The tile with more key tiles
+        // (tile 1 under a causal mask) leads, so both end close together.
+        const int lead = (FA_LEAD_LONGER && w.n1 > w.n0) ? 1 : 0;
+        const int n_lead = lead ? w.n1 : w.n0, n_fol = lead ? w.n0 : w.n1;
+        const int c_lead = lead ? c1 : c0, c_fol = lead ? c0 : c1;
         auto order_bar = [&](int jj) -> uint64_t* {
           if (!FA_SORDER) return nullptr;
-          if (t == 0) return (jj >= 1 && jj - 1 < w.n1) ? s_full + 1 : nullptr;
-          return (jj < w.n0) ? s_full + 0 : nullptr;
+          if (t == lead) return (jj >= 1 && jj - 1 < n_fol) ? s_full + (1 - lead) : nullptr;
+          return (jj < n_lead) ? s_full + lead : nullptr;
         };
         auto order_par = [&](int jj) -> uint32_t {
-          return static_cast<uint32_t>((t == 0 ? c1 + jj - 1 : c0 + jj) & 1);
+          return static_cast<uint32_t>((t == lead ? c_fol + jj - 1 : c_lead + jj) & 1);
         };
         // (The first PV of a unit overwrites O_t, which the previous unit's
         // epilogue read: that is implied by p_full of the unit's first step,
         // which the softmax arrives on only after that epilogue.)
 
-        // Ping-pong: the second Q tile starts once the first tile's first
+        // Ping-pong: the following Q tile starts once the leader's first
         // softmax is done, so one tile's exponentials overlap the other tile's
         // MMAs instead of both tiles competing for the same unit at once.
-        if (C::STAGGER && t == 1 && w.n0 >= FA_STAGGER_MIN_TILES && nt > 0 && !wait_bar(p_full + 0, c0 & 1)) break;
+        if (C::STAGGER && t != lead && n_lead >= FA_STAGGER_MIN_TILES && nt > 0 &&
+            !wait_bar(p_full + lead, c_lead & 1))
+          break;
 
         if (C::SEP_P) {
           // Software pipeline: S_{j+1} is issued as soon as the softmax has
