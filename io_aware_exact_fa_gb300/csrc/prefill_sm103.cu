@@ -711,16 +711,25 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         }
         // tiles whose 128 keys are all kept for every row of the warp skip the
         // element-wise mask (warp-uniform choice of code path)
-        const bool need_mask = (kbase + BLOCK_N > p.Nk) || (p.causal && kbase + BLOCK_N - 1 > tile_lim) ||
-                               !__all_sync(0xffffffffu, keep_all);
+        const bool all_kept = __all_sync(0xffffffffu, keep_all) != 0;
+        const bool need_mask = (kbase + BLOCK_N > p.Nk) || (p.causal && kbase + BLOCK_N - 1 > tile_lim) || !all_kept;
         if (need_mask) {
+          if (all_kept) {
+            // every key of the tile kept: keys past min(Nk - 1, diag) are
+            // hidden, a threshold (much cheaper than testing mask bits)
+            const int lim = min(p.causal ? diag : INT_MAX, p.Nk - 1) - kbase;  // last visible column
 #pragma unroll
-          for (int c = 0; c < BLOCK_N; ++c) {
-            const int key = kbase + c;
-            bool vis = key < p.Nk;
-            if (p.causal) vis = vis && key <= diag;
-            vis = vis && ((kw[c >> 5] >> (c & 31)) & 1u);
-            if (!vis) s[c] = f2u(-INFINITY);
+            for (int c = 0; c < BLOCK_N; ++c)
+              if (c > lim) s[c] = f2u(-INFINITY);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BLOCK_N; ++c) {
+              const int key = kbase + c;
+              bool vis = key < p.Nk;
+              if (p.causal) vis = vis && key <= diag;
+              vis = vis && ((kw[c >> 5] >> (c & 31)) & 1u);
+              if (!vis) s[c] = f2u(-INFINITY);
+            }
           }
         }
         // row max: 8 independent chains of three-input maxima, then a short tree
