@@ -18,6 +18,9 @@ Every function restates what the pages compute, in fp64, with NumPy:
   pages' worked examples with their intermediate states.
 * ``merge_partials`` / ``splitkv_attention`` -- the two-block merge identity
   applied to per-split (m, l, o) triples, the arithmetic of split-KV decode.
+* ``attention_grad.attend_head_grad`` / ``attention_grad.attention_grad`` --
+  the backward pass: gradients of a loss through O with respect to Q, K and V
+  (the chain rule through the definition, with the exact P).
 
 Pins (tests/test_oracle.py): the pages' worked examples (tests/golden/),
 agreement with torch's fp64 ``scaled_dot_product_attention`` and with
