@@ -135,6 +135,32 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
 fa_status fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                                     int B, int H, int Nk, int d, float scale, int num_splits, void* stream);
 
+/* Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator
+ * [B, H, Nq, d] and two fp32 per-row statistics [B, H, Nq], each rounded up
+ * to 256 bytes. Returns 0 for invalid arguments. */
+size_t fa_bwd_workspace_size(int B, int H, int Nq, int d);
+
+/* Backward pass of fa_fwd (no key mask): given dout = dL/dO, writes
+ * dq = dL/dQ, dk = dL/dK and dv = dL/dV for the same q, k, v, scale and
+ * causal flag. The probability tiles are recomputed from the forward's lse
+ * instead of being stored ("Flash Attention Optimization", section "Sizing a
+ * tile, and why the backward pass recomputes instead of storing"; "Explain
+ * FlashAttention ...", section "Exact attention, finite precision and
+ * backward"): with P = exp(scale Q K^T - lse) over the visible keys and
+ * D_i = sum_c dout_ic o_ic,
+ *   dv = P^T dout,  dS = P * (dout V^T - D),  dq = scale dS K,  dk = scale dS^T Q.
+ *   q, o, dout, dq  bf16 [B, H, Nq, d]     k, v, dk, dv  bf16 [B, H, Nk, d]
+ *   lse             fp32 [B, H, Nq], as written by fa_fwd for these inputs
+ *   workspace       device memory of at least fa_bwd_workspace_size() bytes,
+ *                   256-byte aligned, owned by the caller; overwritten.
+ * Requires B, H, Nq, Nk >= 1, d in {64, 128}, 16-byte aligned bf16 buffers,
+ * a finite scale >= 0. Keys no visible query reaches get dk = dv = 0. Three
+ * launches on `stream` (statistics, the fused tiles, dq conversion); errors
+ * as for fa_fwd, plus FA_ERR_WORKSPACE. */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_ERR_TIMEOUT if a bounded wait gave up since the
  * last call, FA_ERR_CUDA if the stream reported an error, else FA_OK. */

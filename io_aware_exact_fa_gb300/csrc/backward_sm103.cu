@@ -1,0 +1,500 @@
+// Exact-attention backward pass for sm_103a: dQ, dK, dV of a loss through
+// O = softmax(scale * Q K^T + causal mask) V, recomputing the probability
+// tiles from the forward's per-row log-sum-exp instead of storing P ("Flash
+// Attention Optimization", section "Sizing a tile, and why the backward pass
+// recomputes instead of storing"; "Explain FlashAttention ...", section
+// "Exact attention, finite precision and backward"). With
+// P_ij = exp(scale q_i.k_j - lse_i) and D_i = sum_c dO_ic O_ic:
+//   dV = P^T dO,   dS = P * (dO V^T - D),   dQ = scale dS K,   dK = scale dS^T Q.
+//
+// Three launches:
+//   fa_bwd_prep_kernel      D and lse (log2 units) per query row; zero the
+//                           fp32 dQ accumulator.
+//   fa_bwd_kernel<D>        one CTA per 128-key tile of one (b, h): K and V stay
+//                           in shared memory while the 128-row Q / dO tiles
+//                           the causal mask leaves visible stream past; dK and
+//                           dV accumulate in TMEM; each Q tile's dQ
+//                           contribution is added to the accumulator with
+//                           vector atomics.
+//   fa_bwd_finish_kernel    dQ = bf16(scale * accumulator).
+//
+// fa_bwd_kernel, 384 threads:
+//   warp 0      TMA producer: K and V once, then Q_i / dO_i into two stages.
+//   warp 1      TMEM allocator and MMA issuer.
+//   warps 4-7   "softmax-grad": each thread owns one key row (TMEM lane) of
+//               S^T = K Q_i^T and dP^T = V dO_i^T, forms P^T and dS^T, writes
+//               P^T (bf16) into the S^T columns and dS^T (bf16) into shared
+//               memory; at the end writes dK and dV.
+//   warps 8-11  dQ drain: each thread owns one query row of dQ_i = dS K.
+// TMEM columns: S^T [0,128) (P^T bf16 in [0,64)), dP^T [128,256) (later
+// dQ_i), dV [256,256+D), dK [256+D,256+2D).
+#include <cuda_bf16.h>
+
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr int BWD_THREADS = 384;
+constexpr int BWD_TMA_WARP = 0;
+constexpr int BWD_MMA_WARP = 1;
+constexpr int BWD_SG_WARP0 = 4;  // warps 4-7
+constexpr int BWD_DQ_WARP0 = 8;  // warps 8-11
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static constexpr int TILE_BYTES = 128 * D * 2;  // one K, V, Q or dO tile (128 rows x D bf16)
+  static constexpr int BOX_BYTES = 128 * 128;     // one TMA box: 128 rows x 64 bf16
+  static constexpr int NBOX = D / 64;
+  static constexpr int DS_BYTES = 128 * 128 * 2;  // dS^T tile: 128 keys x 128 queries bf16
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + TILE_BYTES;
+  static constexpr int Q_OFF = V_OFF + TILE_BYTES;                 // 2 stages of (Q, dO)
+  static constexpr int DS_OFF = Q_OFF + 2 * 2 * TILE_BYTES;
+  static constexpr int STAT_OFF = DS_OFF + DS_BYTES;               // lse2[128], Dv[128]
+  static constexpr int BAR_OFF = STAT_OFF + 2 * 128 * 4;
+  static constexpr int NBAR = 16;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static constexpr uint32_t ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+  static constexpr uint32_t IDESC_T = idesc_bf16_f32(128, 128, false);        // K-major A and B
+  static constexpr uint32_t IDESC_B_MN = idesc_bf16_f32(128, D, true);        // B MN-major
+  static constexpr uint32_t IDESC_AB_MN = idesc_bf16_f32(128, D, true, true); // A and B MN-major
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(a, parity)) return;
+    if ((i & 31u) == 31u && globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+// First 128-row Q tile a key tile starting at key k0 needs under the causal
+// mask: query i sees key j iff j <= i + delta.
+__device__ __forceinline__ int first_qtile(int k0, int delta, bool causal) {
+  if (!causal) return 0;
+  const int first_q = k0 - delta;  // the smallest query that sees key k0
+  return first_q <= 0 ? 0 : first_q / 128;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ prepare
+// One thread per query row: D_i = sum_c dO_ic O_ic (fp32), lse2_i = lse_i *
+// log2(e) (+inf for an empty row, so its recomputed weights are 0), and the
+// row of the fp32 dQ accumulator set to 0.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                          const __nv_bfloat16* __restrict__ dout,
+                                                          const float* __restrict__ lse, float* __restrict__ dq_acc,
+                                                          float* __restrict__ lse2, float* __restrict__ drow,
+                                                          long long rows) {
+  const long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  const uint4* po = reinterpret_cast<const uint4*>(o + r * D);
+  const uint4* pd = reinterpret_cast<const uint4*>(dout + r * D);
+  float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 a = __ldg(po + c), b = __ldg(pd + c);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[e]));
+      const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[e]));
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+  drow[r] = acc;
+  const float l = lse[r];
+  lse2[r] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+  float4* q = reinterpret_cast<float4*>(dq_acc + r * D);
+#pragma unroll
+  for (int c = 0; c < D / 4; ++c) q[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------- finish
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_finish_kernel(const float* __restrict__ dq_acc,
+                                                            __nv_bfloat16* __restrict__ dq, float scale,
+                                                            long long n8) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+  uint4 w;
+  w.x = pack_bf16x2(a.x * scale, a.y * scale);
+  w.y = pack_bf16x2(a.z * scale, a.w * scale);
+  w.z = pack_bf16x2(b.x * scale, b.y * scale);
+  w.w = pack_bf16x2(b.z * scale, b.w * scale);
+  reinterpret_cast<uint4*>(dq)[i] = w;
+}
+
+// --------------------------------------------------------------------- main
+template <int D>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + C::K_OFF;
+  uint8_t* sV = smem + C::V_OFF;
+  uint8_t* sQ0 = smem + C::Q_OFF;  // stage s: Q at Q_OFF + s*2*TILE, dO right after
+  uint8_t* sDS = smem + C::DS_OFF;
+  float* s_lse2 = reinterpret_cast<float*>(smem + C::STAT_OFF);
+  float* s_drow = s_lse2 + 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* q_full = bars + 1;     // [2]
+  uint64_t* q_empty = bars + 3;    // [2]
+  uint64_t* s_full = bars + 5;     // S^T and dP^T of a step computed
+  uint64_t* p_full = bars + 6;     // P^T stored in TMEM and dS^T in shared memory
+  uint64_t* dv_done = bars + 7;    // the step's dV MMA (reading P^T from the S^T columns) completed
+  uint64_t* step_done = bars + 8;  // every MMA of the step completed (dS^T may be rewritten)
+  uint64_t* dq_full = bars + 9;    // dQ_i in the dP^T columns
+  uint64_t* dq_free = bars + 10;   // dQ_i read out
+  uint64_t* acc_done = bars + 11;  // every MMA completed: dK, dV final
+  uint64_t* stat_full = bars + 12; // the step's lse / D staged in shared memory by all 128 threads
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t lim = p.wait_limit_ns;
+  const int nkt = (p.Nk + 127) / 128;
+  const int bh = static_cast<int>(blockIdx.x) / nkt;
+  const int kt = static_cast<int>(blockIdx.x) % nkt;
+  const int k0 = kt * 128;
+  const int delta = p.Nk - p.Nq;
+  const int nqt = (p.Nq + 127) / 128;
+  const int qt0 = first_qtile(k0, delta, p.causal != 0);
+  const int n_it = max(0, nqt - qt0);  // Q tiles this key tile visits
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(q_full + s, 1);
+      mbar_init(q_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(dv_done, 1);
+    mbar_init(step_done, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(stat_full, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == BWD_MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == BWD_TMA_WARP) {
+    // ---------------------------------------------------------- TMA producer
+    const bool leader = lane == 0;
+    bool ok = true;
+    int issued = 0;
+    if (leader) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE_BYTES);
+      for (int b = 0; b < C::NBOX; ++b) {
+        tma_load_3d(sK + b * C::BOX_BYTES, &tmK, kv_full, 64 * b, k0, bh);
+        tma_load_3d(sV + b * C::BOX_BYTES, &tmV, kv_full, 64 * b, k0, bh);
+      }
+    }
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it & 1;
+      if (it >= 2) {
+        ok = mbar_wait(q_empty + s, ((it - 2) >> 1) & 1, lim, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      if (leader) {
+        uint8_t* dq_ = sQ0 + s * 2 * C::TILE_BYTES;
+        const int q0 = (qt0 + it) * 128;
+        mbar_arrive_expect_tx(q_full + s, 2 * C::TILE_BYTES);
+        for (int b = 0; b < C::NBOX; ++b) {
+          tma_load_3d(dq_ + b * C::BOX_BYTES, &tmQ, q_full + s, 64 * b, q0, bh);
+          tma_load_3d(dq_ + C::TILE_BYTES + b * C::BOX_BYTES, &tmDO, q_full + s, 64 * b, q0, bh);
+        }
+      }
+      ++issued;
+    }
+    if (leader) {
+      // every copy issued lands before the CTA exits
+      mbar_drain(kv_full, 0, lim);
+      for (int n = max(0, issued - 2); n < issued; ++n) mbar_drain(q_full + (n & 1), (n >> 1) & 1, lim);
+    }
+    __syncwarp();
+  } else if (warp == BWD_MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = lane == 0;
+    bool ok = true;
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+      ok = mbar_wait(bar, parity, lim, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      return ok;
+    };
+    constexpr uint32_t DHI = sdesc_sw128_hi(1024);
+    const uint32_t k_lo = sdesc_sw128_lo(smem_u32(sK), 16), kmn_lo = sdesc_sw128_lo(smem_u32(sK), C::BOX_BYTES);
+    const uint32_t v_lo = sdesc_sw128_lo(smem_u32(sV), 16);
+    const uint32_t ds_lo = sdesc_sw128_lo(smem_u32(sDS), 16), dsmn_lo = sdesc_sw128_lo(smem_u32(sDS), C::BOX_BYTES);
+    const uint32_t tST = tmem + C::ST_COL, tDPT = tmem + C::DPT_COL, tDV = tmem + C::DV_COL,
+                   tDK = tmem + C::DK_COL;
+    // K-major K-step kk of a tile: (kk / 4) boxes plus (kk % 4) x 32 bytes in;
+    // MN-major K-step kk: 16 rows = 2048 bytes in (64-column boxes LBO apart)
+    auto kmaj = [](int kk) { return static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
+    auto mnmaj = [](int kk) { return static_cast<uint32_t>((kk * 2048) >> 4); };
+    if (n_it > 0 && !wait_bar(kv_full, 0)) ok = false;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it & 1;
+      const uint32_t q_base = smem_u32(sQ0) + s * 2 * C::TILE_BYTES;
+      const uint32_t q_lo = sdesc_sw128_lo(q_base, 16), qmn_lo = sdesc_sw128_lo(q_base, C::BOX_BYTES);
+      const uint32_t do_lo = sdesc_sw128_lo(q_base + C::TILE_BYTES, 16),
+                     domn_lo = sdesc_sw128_lo(q_base + C::TILE_BYTES, C::BOX_BYTES);
+      if (!wait_bar(q_full + s, (it >> 1) & 1)) break;
+      // S^T (the S^T columns) is rewritten only after the previous dV read P^T there
+      if (it > 0 && !wait_bar(dv_done, (it - 1) & 1)) break;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_w(tST, k_lo + kmaj(kk), DHI, q_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
+      }
+      // dP^T (the dP^T columns) only after the previous dQ_i was read out
+      if (it > 0 && !wait_bar(dq_free, (it - 1) & 1)) break;
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_w(tDPT, v_lo + kmaj(kk), DHI, do_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
+        mma_commit(s_full);
+      }
+      if (!wait_bar(p_full, it & 1)) break;
+      if (leader) {
+        // dV += P^T dO_i (A = P^T from TMEM, B = dO_i MN-major)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts_w(tDV, tST + kk * 8, domn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(dv_done);
+        // dK += dS^T Q_i (A = dS^T K-major, B = Q_i MN-major)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_w(tDK, ds_lo + kmaj(kk), DHI, qmn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
+        // dQ_i = dS K (A = dS, the MN-major view of dS^T; B = K MN-major), into the dP^T columns
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_w(tDPT, dsmn_lo + mnmaj(kk), DHI, kmn_lo + mnmaj(kk), DHI, C::IDESC_AB_MN, kk > 0 ? 1u : 0u);
+        mma_commit(dq_full);
+        mma_commit(step_done);
+        mma_commit(q_empty + s);
+      }
+    }
+    if (leader) {
+      if (n_it > 0) mma_commit(acc_done);
+      else mbar_arrive(acc_done);
+      mbar_drain(acc_done, 0, lim);  // every MMA completed before TMEM is released
+    }
+    __syncwarp();
+  } else if (warp >= BWD_SG_WARP0 && warp < BWD_SG_WARP0 + 4) {
+    // ---------------------------------------------------------- softmax-grad
+    const int wq = warp - BWD_SG_WARP0;
+    const int row = wq * 32 + lane;  // key row within the tile
+    const int kabs = k0 + row;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tST = tmem + lane_base + C::ST_COL, tDPT = tmem + lane_base + C::DPT_COL;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    const uint32_t ds_row = smem_u32(sDS) + static_cast<uint32_t>(row) * 128u;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int q0 = (qt0 + it) * 128;
+      ok = mbar_wait(s_full, it & 1, lim, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // this Q tile's lse (log2 units) and D into shared memory; every thread of
+      // the previous step has finished with them (s_full needed all of p_full)
+      {
+        const int qi = q0 + row;
+        const size_t gi = static_cast<size_t>(bh) * p.Nq + qi;
+        s_lse2[row] = qi < p.Nq ? p.lse2[gi] : INFINITY;
+        s_drow[row] = qi < p.Nq ? p.drow[gi] : 0.f;
+      }
+      mbar_arrive(stat_full);  // release: this thread's two values are visible to the waiters
+      ok = mbar_wait(stat_full, it & 1, lim, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      // dS^T in shared memory is rewritten only after the previous step's dK and dQ read it
+      if (it > 0) {
+        ok = mbar_wait(step_done, (it - 1) & 1, lim, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      // visible queries of this key row: q >= kabs - delta (causal), q < Nq, kabs < Nk
+      const int q_lo_vis = p.causal ? kabs - delta : INT_MIN;
+      const bool key_ok = kabs < p.Nk;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tST + ch * 32, sv);
+        tmem_ld32(tDPT + ch * 32, dp);
+        tmem_ld_wait32(sv);
+        reg_fence32(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pr[2], dsr[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = ch * 32 + 2 * i + h;
+            const int qabs = q0 + c;
+            const bool vis = key_ok && qabs >= q_lo_vis && qabs < p.Nq;
+            const float e = ex2_approx(fmaf(u2f(sv[2 * i + h]), sl2, -s_lse2[c]));
+            const float pp = vis ? e : 0.f;
+            pr[h] = pp;
+            dsr[h] = pp * (u2f(dp[2 * i + h]) - s_drow[c]);
+          }
+          pk[i] = pack_bf16x2(pr[0], pr[1]);
+          dk[i] = pack_bf16x2(dsr[0], dsr[1]);
+        }
+        tmem_st16(tST + ch * 16, pk);  // P^T over S^T columns already read
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int cc = ch * 4 + v;  // 16-byte chunk of the dS^T row: box cc / 8, chunk cc % 8
+          const uint32_t a = ds_row + static_cast<uint32_t>((cc >> 3) * C::BOX_BYTES) +
+                             (static_cast<uint32_t>((cc & 7) ^ (row & 7)) << 4);
+          st_shared_v4(a, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    // ---- epilogue: dK = scale * acc, dV = acc (bf16), rows below Nk
+    if (ok) {
+      ok = mbar_wait(acc_done, 0, lim, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    // tcgen05.ld is warp-collective: every lane loads, only rows below Nk store
+    if (ok) {
+      const bool row_ok = kabs < p.Nk;
+      const size_t kr = static_cast<size_t>(bh) * p.Nk + (row_ok ? kabs : 0);
+      __nv_bfloat16* dvr = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
+      __nv_bfloat16* dkr = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t src = tmem + lane_base + (which ? C::DK_COL : C::DV_COL);
+        const float f = which ? p.scale : 1.f;
+        __nv_bfloat16* dst = which ? dkr : dvr;
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t a[32];
+          if (n_it > 0) {
+            tmem_ld32(src + ch * 32, a);
+            tmem_ld_wait32(a);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = 0u;
+          }
+          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            if (row_ok) d4[v] = make_uint4(pack_bf16x2(u2f(a[8 * v]) * f, u2f(a[8 * v + 1]) * f),
+                               pack_bf16x2(u2f(a[8 * v + 2]) * f, u2f(a[8 * v + 3]) * f),
+                               pack_bf16x2(u2f(a[8 * v + 4]) * f, u2f(a[8 * v + 5]) * f),
+                               pack_bf16x2(u2f(a[8 * v + 6]) * f, u2f(a[8 * v + 7]) * f));
+        }
+      }
+    }
+  } else if (warp >= BWD_DQ_WARP0) {
+    // -------------------------------------------------------------- dQ drain
+    const int wq = warp - BWD_DQ_WARP0;
+    const int row = wq * 32 + lane;  // query row within the Q tile
+    const uint32_t src = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::DPT_COL;
+    bool ok = true;
+    for (int it = 0; ok && it < n_it; ++it) {
+      ok = mbar_wait(dq_full, it & 1, lim, p.status, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int qabs = (qt0 + it) * 128 + row;
+      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qabs) * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t a[32];
+        tmem_ld32(src + ch * 32, a);
+        tmem_ld_wait32(a);
+        if (qabs < p.Nq) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            red_add_v4_f32(dst + ch * 32 + 4 * v, u2f(a[4 * v]), u2f(a[4 * v + 1]), u2f(a[4 * v + 2]),
+                           u2f(a[4 * v + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == BWD_MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
+                                const float* lse, void* dq, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, p.dq_acc, p.lse2,
+      p.drow, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long ctas = static_cast<long long>(p.B) * p.H * ((p.Nk + 127) / 128);
+  fa_bwd_kernel<D><<<static_cast<unsigned>(ctas), BWD_THREADS, BwdCfg<D>::SMEM, stream>>>(tq, tk, tv, tdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const long long n8 = rows * D / 8;
+  fa_bwd_finish_kernel<D><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+      p.dq_acc, static_cast<__nv_bfloat16*>(dq), p.scale, n8);
+  return cudaGetLastError();
+}
+
+cudaError_t bwd_set_attributes(int d) {
+  if (d == 64)
+    return cudaFuncSetAttribute(fa_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<64>::SMEM);
+  return cudaFuncSetAttribute(fa_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<128>::SMEM);
+}
+
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout, const float* lse,
+                       void* dq, cudaStream_t stream) {
+  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, p, o, dout, lse, dq, stream)
+                 : launch_bwd_t<128>(tq, tk, tv, tdo, p, o, dout, lse, dq, stream);
+}
+
+}  // namespace fa

@@ -79,6 +79,8 @@ fa_status device_state(DeviceState** out) {
     st.status = static_cast<unsigned int*>(p);
     if ((e = fa::prefill_set_attributes(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
     if ((e = fa::prefill_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
+    if ((e = fa::bwd_set_attributes(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=64)");
+    if ((e = fa::bwd_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=128)");
     // The in-kernel register split assumes this launch allocation; a
     // different one could make setmaxnreg.inc wait forever, so refuse.
     for (int d : {64, 128}) {
@@ -270,6 +272,68 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
   cudaError_t e = fa::launch_decode(d, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   t_launches += 2;
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int Nq, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Nq;
+  const size_t acc = (rows * d * 4 + 255) & ~size_t(255);
+  const size_t stat = (rows * 4 + 255) & ~size_t(255);
+  return acc + 2 * stat;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  t_detail[0] = 0;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1)
+    return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Nq >= 1, Nk >= 1 (got %d %d %d %d)", B, H, Nq, Nk);
+  if (fa_status s = check_scale(scale)) return s;
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv)
+    return fail(FA_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk and dv must be non-NULL");
+  const long long BH = static_cast<long long>(B) * H;
+  const long long ctas = BH * ((Nk + 127) / 128);
+  if (BH > INT_MAX || ctas > INT_MAX || BH * Nq > (1LL << 40))
+    return fail(FA_ERR_INVALID_ARG, "B*H or the grid is too large");
+  for (const void* ptr : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                          static_cast<const void*>(dv)})
+    if (!aligned(ptr, 16)) return fail(FA_ERR_UNSUPPORTED, "q, k, v, o, dout, dq, dk, dv must be 16-byte aligned");
+  if (!aligned(lse, 4)) return fail(FA_ERR_UNSUPPORTED, "lse must be 4-byte aligned");
+  const size_t need = fa_bwd_workspace_size(B, H, Nq, d);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", need);
+
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  CUtensorMap tq, tk, tv, tdo;
+  if (fa_status s = encode_map(&tq, q, Nq, static_cast<int>(BH), d)) return s;
+  if (fa_status s = encode_map(&tk, k, Nk, static_cast<int>(BH), d)) return s;
+  if (fa_status s = encode_map(&tv, v, Nk, static_cast<int>(BH), d)) return s;
+  if (fa_status s = encode_map(&tdo, dout, Nq, static_cast<int>(BH), d)) return s;
+  const size_t rows = static_cast<size_t>(BH) * Nq;
+  const size_t acc = (rows * d * 4 + 255) & ~size_t(255);
+  const size_t stat = (rows * 4 + 255) & ~size_t(255);
+  fa::BwdParams p{};
+  p.dq_acc = static_cast<float*>(workspace);
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc);
+  p.drow = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc + stat);
+  p.dk = dk;
+  p.dv = dv;
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  // as in the forward pass, scale 0 runs with the smallest normal multiplier
+  p.scale_log2 = fmaxf(scale * 1.4426950408889634f, 1.17549435e-38f);
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.status = st->status;
+  cudaError_t e = fa::launch_bwd(d, tq, tk, tv, tdo, p, o, dout, lse, dq, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  t_launches += 3;
   return FA_OK;
 }
 

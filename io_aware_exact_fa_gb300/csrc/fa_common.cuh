@@ -66,6 +66,20 @@ struct PrefillParams {
   int split_from;            // units from here on are single tiles of the last pairs
 };
 
+struct BwdParams {
+  float* dq_acc;             // fp32 [B*H, Nq, d] workspace: dQ / scale, accumulated
+  float* lse2;               // fp32 [B*H, Nq] workspace: lse * log2(e) (+inf for an empty row)
+  float* drow;               // fp32 [B*H, Nq] workspace: sum_c dO * O per row
+  void* dk;                  // bf16 [B*H, Nk, d]
+  void* dv;                  // bf16 [B*H, Nk, d]
+  int B, H, Nq, Nk;
+  int causal;
+  float scale;               // softmax scale
+  float scale_log2;          // scale * log2(e)
+  uint64_t wait_limit_ns;
+  unsigned int* status;      // device status word
+};
+
 struct DecodeParams {
   const void* q;             // bf16 [B*H, d]
   const void* k;             // bf16 [B*H, Nk, d]
@@ -85,6 +99,10 @@ size_t prefill_smem_bytes(int d);
 cudaError_t prefill_set_attributes(int d);
 int prefill_num_regs(int d);   // registers per thread the prefill kernel launches with
 cudaError_t launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout, const float* lse,
+                       void* dq, cudaStream_t stream);
+cudaError_t bwd_set_attributes(int d);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int* status, cudaStream_t stream);
 cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream);
 

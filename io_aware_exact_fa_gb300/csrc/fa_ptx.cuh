@@ -183,8 +183,8 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
 //   (1 = bf16), 15 A major (0 = K), 16 B major (0 = K, 1 = MN),
 //   17-22 N >> 3, 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major, bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -362,6 +362,12 @@ __device__ __forceinline__ uint64_t exp2_fma2(uint64_t x) {
   const float r0 = __uint_as_float((__float_as_uint(t0) << 23) + __float_as_uint(p0));
   const float r1 = __uint_as_float((__float_as_uint(t1) << 23) + __float_as_uint(p1));
   return f2pack(r0, r1);
+}
+
+// Vector atomic add of four fp32 values at a 16-byte-aligned global address.
+__device__ __forceinline__ void red_add_v4_f32(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

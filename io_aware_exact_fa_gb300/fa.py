@@ -40,6 +40,8 @@ EXPORTS = {
     "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_decode_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_decode_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
     "fa_set_wait_limit_ns": (None, [_u64]),
     "fa_get_wait_limit_ns": (_u64, []),
@@ -180,6 +182,36 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                                         int(num_splits), _stream_ptr(stream))
     _check(rc, "fa_decode_splitkv_noalloc")
     return out, lse
+
+
+def bwd_workspace_size(B: int, H: int, Nq: int, d: int) -> int:
+    return int(_lib.fa_bwd_workspace_size(B, H, Nq, d))
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+        dout: torch.Tensor, scale: Optional[float] = None, causal: bool = False,
+        workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Backward pass of ``fwd`` (no key mask): returns (dq, dk, dv), bf16, shaped like q, k, v."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _need(t, n)
+    _need(lse, "lse", torch.float32)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != (B, H, Nk, d) or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shapes: q, o, dout [B,H,Nq,d]; k, v [B,H,Nk,d]")
+    if lse.shape != (B, H, Nq):
+        raise ValueError("lse must be [B, H, Nq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = bwd_workspace_size(B, H, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    rc = _lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+                     workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(rc, "fa_bwd")
+    return dq, dk, dv
 
 
 def device_status(stream: Optional[torch.cuda.Stream] = None) -> int:
