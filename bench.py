@@ -127,9 +127,15 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = self.samples
-        if self.window:
-            inside = [r for r in rows if self.window[0] - 0.06 <= r[0] <= self.window[1] + 0.06]
+        return self.summary(self.window)
+
+    def summary(self, window=None):
+        """Median SM clock, max clock and throttle reasons seen inside ``window`` (wall-clock seconds)."""
+        if self.proc is None:
+            return None
+        rows = list(self.samples)
+        if window:
+            inside = [r for r in rows if window[0] - 0.06 <= r[0] <= window[1] + 0.06]
             rows = inside or rows
         if not rows:
             return None
@@ -180,6 +186,75 @@ def oracle_prefill_sample(w, budget_s: float):
             return flops, el, heads
 
 
+def run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, world, rank, dev):
+    """Time fa_bwd (prep + main + finish launches) on the prefill workload's
+    inputs, once per causal mode per step, with its own events and L2 flush;
+    dO is seeded N(0,1) bf16 and O, lse come from the forward pass."""
+    import torch
+    import torch.distributed as dist
+    gen = torch.Generator().manual_seed(2000 + rank)
+    dout = torch.randn(tuple(q.shape), generator=gen).to(torch.bfloat16).to(dev)
+    fo = {}
+    for c in modes:
+        fo[c] = (torch.empty_like(q), torch.empty(tuple(lse.shape), dtype=torch.float32, device=dev))
+        fa.fwd(q, k, v, scale=wp.scale, causal=c, out=fo[c][0], lse=fo[c][1])
+    wsb = torch.empty(max(1, fa.bwd_workspace_size(wp.B, wp.H, wp.Nq, wp.d)), dtype=torch.uint8, device=dev)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+
+    def backward(c):
+        fa.bwd(q, k, v, fo[c][0], fo[c][1], dout, scale=wp.scale, causal=c, workspace=wsb, grads=grads)
+
+    for _ in range(warm):
+        flush.zero_()
+        for c in modes:
+            backward(c)
+    torch.cuda.synchronize()
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError("device status not OK after the backward warm-up")
+    K, nm = args.steps, len(modes)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nm + 1)] for _ in range(K)]
+    n0 = fa.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, c in enumerate(modes):
+            backward(c)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    launches = fa.launch_count() - n0
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError("device status not OK after the backward timed region")
+    tm = torch.tensor([sum(e[j].elapsed_time(e[j + 1]) for e in ev) / 1e3 for j in range(nm)],
+                      dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+    tm = tm.tolist()
+    fm = [wp.bwd_flops(c) for c in modes]
+    ach = K * sum(fm) / sum(tm) / 1e12
+    peaks = measured_peaks()
+    out = {"value": world * ach, "unit": "TFLOP/s", "ms": sum(tm) / K * 1e3, "gpu_launches": launches,
+           "dout": "N(0,1) bf16, seeded; O and lse from fa_fwd",
+           "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": ach / peaks["bf16_tflops"],
+                        "traffic": recorded_traffic("backward_sm103.cu", wp.name + "_bwd"),
+                        "kernel": f"fa_bwd_kernel<{wp.d}> (+ fa_bwd_prep_kernel, fa_bwd_finish_kernel)",
+                        "peak_source": f"{peaks['source']} bf16 burst",
+                        "flop_convention": "10*B*H*Nq*Nk*d per non-causal launch (five products), halved for causal"},
+           "_window": (t0, t1)}
+    for c, t, f in zip(modes, tm, fm):
+        tag = "causal" if c else "noncausal"
+        out["roofline"][f"ms_{tag}"] = t / K * 1e3
+        out["roofline"][f"tflops_{tag}"] = K * f / t / 1e12
+    return out
+
+
 # --------------------------------------------------------------- reference
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -222,8 +297,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline (0 = skip)")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "backward"],
                     help="run one part of the step only (small profiling runs)")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward-pass leg (timed after the step, reported under 'backward')")
     ap.add_argument("--decode-b", type=int, default=0, help="override the decode batch (profiling a small case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--prefill-workload", default=PREFILL,
@@ -251,12 +328,14 @@ def main():
     do_p = args.only in ("all", "prefill")
     do_d = args.only in ("all", "decode")
     wp = W.WORKLOADS[args.prefill_workload]
+    # the backward pass takes no key mask: it is timed on the unpadded workloads
+    do_b = args.only in ("all", "backward") and not args.no_backward and not wp.pad_heads
     modes = list(wp.causal_modes)
     wd = W.WORKLOADS[DECODE]
     if args.decode_b:
         import dataclasses
         wd = dataclasses.replace(wd, B=args.decode_b, name=wd.name.replace("b64", f"b{args.decode_b}"))
-    if do_p:
+    if do_p or do_b:
         q, k, v = W.make_qkv(wp.B, wp.H, wp.Nq, wp.Nk, wp.d, seed=rank, device="cuda")
         o = torch.empty_like(q)
         lse = torch.empty(wp.B, wp.H, wp.Nq, dtype=torch.float32, device=dev)
@@ -320,10 +399,13 @@ def main():
         dist.barrier()
     t_wall1 = time.time()
     launches = fa.launch_count() - launches0
-    sampler.mark(t_wall0, t_wall1)
-    clocks = sampler.stop()
     if fa.device_status() != fa.FA_OK:
         raise RuntimeError("device status not OK after the timed region")
+    bwd = run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, world, rank, dev) if do_b else None
+    sampler.stop()
+    clocks = sampler.summary((t_wall0, t_wall1))
+    if bwd is not None:
+        bwd["clocks"] = sampler.summary(bwd.pop("_window"))
 
     nm = len(modes)
     t_modes = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / 1e3 for i in range(nm)]
@@ -449,6 +531,10 @@ def main():
                           "e2e": dec_e2e}
         if not do_p:
             line["value"], line["unit"] = line["decode"]["value"], "GB/s"
+    if bwd is not None:
+        line["backward"] = bwd
+        if not do_p and not do_d:
+            line["value"] = bwd["value"]
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -190,8 +190,10 @@ def bwd_workspace_size(B: int, H: int, Nq: int, d: int) -> int:
 
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
         dout: torch.Tensor, scale: Optional[float] = None, causal: bool = False,
-        workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
-    """Backward pass of ``fwd`` (no key mask): returns (dq, dk, dv), bf16, shaped like q, k, v."""
+        workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+        grads: Optional[Tuple[torch.Tensor, torch.Tensor, torch.Tensor]] = None):
+    """Backward pass of ``fwd`` (no key mask): returns (dq, dk, dv), bf16, shaped like q, k, v
+    (written into ``grads`` when given)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _need(t, n)
     _need(lse, "lse", torch.float32)
@@ -206,7 +208,14 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     need = bwd_workspace_size(B, H, Nq, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if grads is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = grads
+        for t, ref, n in ((dq, q, "dq"), (dk, k, "dk"), (dv, v, "dv")):
+            _need(t, n)
+            if t.shape != ref.shape:
+                raise ValueError(f"{n} must be shaped like its input")
     rc = _lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, float(scale), int(bool(causal)),
                      workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))

@@ -39,6 +39,11 @@ class Workload:
         f = 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
         return f / 2 if causal else f
 
+    def bwd_flops(self, causal: bool) -> float:
+        """Algorithmic FLOPs of the backward pass's five products (S recomputed,
+        dP, dV, dK, dQ, each 2*Nq*Nk*d per head): 2.5x the forward's, halved for causal."""
+        return 2.5 * self.flops(causal)
+
     def io_bytes(self) -> int:
         """Minimum HBM bytes: Q, K, V read once and O written once (2-byte
         elements) plus the fp32 per-row log-sum-exp."""

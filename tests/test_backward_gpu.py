@@ -123,3 +123,24 @@ def test_backward_rejects(fa):
     with pytest.raises(fa.FAError) as e:
         fa.bwd(y, y, y, y, lse, y, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == fa.FA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("name", ["prefill_2k", "prefill_8k"])
+def test_backward_full_size(fa, name):
+    """The workloads the benchmark's backward leg times, with its inputs (q, k, v
+    seed 0, dO seed 2000): every gradient of two whole heads per causal mode
+    (first and last (b, h)) against the fp64 oracle."""
+    w = W.WORKLOADS[name]
+    q, k, v = W.make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, seed=0)
+    gen = torch.Generator().manual_seed(2000)
+    do = torch.randn(tuple(q.shape), generator=gen).to(torch.bfloat16)
+    qc, kc, vc, dc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    for causal in w.causal_modes:
+        o, lse = fa.fwd(qc, kc, vc, scale=w.scale, causal=causal)
+        gq, gk, gv = fa.bwd(qc, kc, vc, o, lse, dc, scale=w.scale, causal=causal)
+        torch.cuda.synchronize()
+        assert fa.device_status() == fa.FA_OK
+        for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+            got = [t[b, h].double().cpu().numpy() for t in (gq, gk, gv)]
+            ref = AG.attend_head_grad(q[b, h], k[b, h], v[b, h], do[b, h], w.scale, causal)
+            print(name, causal, (b, h), compare_grads(got, ref, f"{name} causal={causal} head {(b, h)}"))
