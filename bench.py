@@ -302,6 +302,7 @@ def main():
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward-pass leg (timed after the step, reported under 'backward')")
     ap.add_argument("--decode-b", type=int, default=0, help="override the decode batch (profiling a small case)")
+    ap.add_argument("--prefill-h", type=int, default=0, help="override the prefill heads (profiling a small case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--prefill-workload", default=PREFILL,
                     choices=["prefill_2k", "prefill_8k", "prefill_32k", "prefill_32k_pad"],
@@ -328,6 +329,9 @@ def main():
     do_p = args.only in ("all", "prefill")
     do_d = args.only in ("all", "decode")
     wp = W.WORKLOADS[args.prefill_workload]
+    if args.prefill_h:
+        import dataclasses
+        wp = dataclasses.replace(wp, H=args.prefill_h, name=f"{wp.name}_h{args.prefill_h}")
     # the backward pass takes no key mask: it is timed on the unpadded workloads
     do_b = args.only in ("all", "backward") and not args.no_backward and not wp.pad_heads
     modes = list(wp.causal_modes)

@@ -135,9 +135,10 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
 fa_status fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                                     int B, int H, int Nk, int d, float scale, int num_splits, void* stream);
 
-/* Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator
- * [B, H, Nq, d] and two fp32 per-row statistics [B, H, Nq], each rounded up
- * to 256 bytes. Returns 0 for invalid arguments. */
+/* Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator of
+ * B*H*ceil(Nq/128)*128*d elements (Nq padded to whole 128-row tiles) and two
+ * fp32 per-row statistics [B, H, Nq], each rounded up to 256 bytes. Returns 0
+ * for invalid arguments. */
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int d);
 
 /* Backward pass of fa_fwd (no key mask): given dout = dL/dO, writes

@@ -87,55 +87,126 @@ __device__ __forceinline__ int first_qtile(int k0, int delta, bool causal) {
 }  // namespace
 
 // ------------------------------------------------------------------ prepare
-// One thread per query row: D_i = sum_c dO_ic O_ic (fp32), lse2_i = lse_i *
-// log2(e) (+inf for an empty row, so its recomputed weights are 0), and the
-// row of the fp32 dQ accumulator set to 0.
+// One thread per query row of the 128-row-padded Q tiles: the row's entries of
+// the tiled fp32 dQ accumulator set to 0 and, for a row below Nq,
+// D_i = sum_c dO_ic O_ic (fp32) and lse2_i = lse_i * log2(e) (+inf for an
+// empty row, so its recomputed weights are 0).
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                           const __nv_bfloat16* __restrict__ dout,
                                                           const float* __restrict__ lse, float* __restrict__ dq_acc,
                                                           float* __restrict__ lse2, float* __restrict__ drow,
-                                                          long long rows) {
+                                                          long long bh_count, int Nq) {
+  const long long nqt = (Nq + 127) / 128;
   const long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (r >= rows) return;
-  const uint4* po = reinterpret_cast<const uint4*>(o + r * D);
-  const uint4* pd = reinterpret_cast<const uint4*>(dout + r * D);
-  float acc = 0.f;
+  if (r >= bh_count * nqt * 128) return;
+  const long long bh = r / (nqt * 128);
+  const int qq = static_cast<int>(r - bh * nqt * 128);
+  float4* acc = reinterpret_cast<float4*>(dq_acc) + ((bh * nqt + (qq >> 7)) * (D / 4)) * 128 + (qq & 127);
+#pragma unroll
+  for (int c = 0; c < D / 4; ++c) acc[c * 128] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (qq >= Nq) return;
+  const long long gr = bh * Nq + qq;
+  const uint4* po = reinterpret_cast<const uint4*>(o + gr * D);
+  const uint4* pd = reinterpret_cast<const uint4*>(dout + gr * D);
+  float a = 0.f;
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
-    const uint4 a = __ldg(po + c), b = __ldg(pd + c);
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+    const uint4 x = __ldg(po + c), y = __ldg(pd + c);
+    const uint32_t wa[4] = {x.x, x.y, x.z, x.w}, wb[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[e]));
       const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[e]));
-      acc = fmaf(fa.x, fb.x, acc);
-      acc = fmaf(fa.y, fb.y, acc);
+      a = fmaf(fa.x, fb.x, a);
+      a = fmaf(fa.y, fb.y, a);
     }
   }
-  drow[r] = acc;
-  const float l = lse[r];
-  lse2[r] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
-  float4* q = reinterpret_cast<float4*>(dq_acc + r * D);
-#pragma unroll
-  for (int c = 0; c < D / 4; ++c) q[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  drow[gr] = a;
+  const float l = lse[gr];
+  lse2[gr] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
 }
 
 // ------------------------------------------------------------------- finish
+// One thread per 8 columns of a dQ row: dQ = bf16(scale * accumulator), read
+// from the tiled accumulator layout.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_finish_kernel(const float* __restrict__ dq_acc,
                                                             __nv_bfloat16* __restrict__ dq, float scale,
-                                                            long long n8) {
+                                                            long long n8, int Nq) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
-  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+  const long long row = i / (D / 8);
+  const int g = static_cast<int>(i - row * (D / 8));
+  const long long bh = row / Nq;
+  const int q = static_cast<int>(row - bh * Nq);
+  const long long nqt = (Nq + 127) / 128;
+  const float4* a4 =
+      reinterpret_cast<const float4*>(dq_acc) + ((bh * nqt + (q >> 7)) * (D / 4) + 2 * g) * 128 + (q & 127);
+  const float4 a = a4[0], b = a4[128];
   uint4 w;
   w.x = pack_bf16x2(a.x * scale, a.y * scale);
   w.y = pack_bf16x2(a.z * scale, a.w * scale);
   w.z = pack_bf16x2(b.x * scale, b.y * scale);
   w.w = pack_bf16x2(b.z * scale, b.w * scale);
   reinterpret_cast<uint4*>(dq)[i] = w;
+}
+
+// --------------------------------------------------------- softmax-grad tile
+// One thread, one key row of a 128 x 128 step: P^T = exp2(S^T * scale * log2(e)
+// - lse2) and dS^T = P^T * (dP^T - D) for the 128 queries of the Q tile. P^T
+// (bf16) goes over the S^T columns already read, dS^T (bf16) into the
+// 128-byte-swizzled shared tile (two 64-column boxes). nlse2 and ndrow hold
+// -lse2 and -D per query column. With MASK, columns below c_lo are masked.
+template <int D, bool MASK>
+__device__ __forceinline__ void sg_tile(uint32_t tST, uint32_t tDPT, uint32_t ds_row, int row, int c_lo,
+                                        const float* nlse2, const float* ndrow, float sl2) {
+  using C = BwdCfg<D>;
+  const uint64_t sl2x2 = f2pack(sl2, sl2);
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t sv[32], dp[32];
+    tmem_ld32(tST + ch * 32, sv);
+    tmem_ld32(tDPT + ch * 32, dp);
+    tmem_ld_wait32(sv);
+    reg_fence32(dp);
+    uint32_t pk[16], dk[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = ch * 32 + 4 * j;
+      const float4 nl = *reinterpret_cast<const float4*>(nlse2 + c);
+      const float4 nd = *reinterpret_cast<const float4*>(ndrow + c);
+      const uint64_t a01 = ffma2(f2pack(u2f(sv[4 * j]), u2f(sv[4 * j + 1])), sl2x2, f2pack(nl.x, nl.y));
+      const uint64_t a23 = ffma2(f2pack(u2f(sv[4 * j + 2]), u2f(sv[4 * j + 3])), sl2x2, f2pack(nl.z, nl.w));
+      float x0, x1, x2, x3;
+      f2unpack(a01, x0, x1);
+      f2unpack(a23, x2, x3);
+      float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+      if (MASK) {
+        p0 = c >= c_lo ? p0 : 0.f;
+        p1 = c + 1 >= c_lo ? p1 : 0.f;
+        p2 = c + 2 >= c_lo ? p2 : 0.f;
+        p3 = c + 3 >= c_lo ? p3 : 0.f;
+      }
+      const uint64_t g01 = fadd2(f2pack(u2f(dp[4 * j]), u2f(dp[4 * j + 1])), f2pack(nd.x, nd.y));
+      const uint64_t g23 = fadd2(f2pack(u2f(dp[4 * j + 2]), u2f(dp[4 * j + 3])), f2pack(nd.z, nd.w));
+      float d0, d1, d2, d3;
+      f2unpack(fmul2(f2pack(p0, p1), g01), d0, d1);
+      f2unpack(fmul2(f2pack(p2, p3), g23), d2, d3);
+      pk[2 * j] = pack_bf16x2(p0, p1);
+      pk[2 * j + 1] = pack_bf16x2(p2, p3);
+      dk[2 * j] = pack_bf16x2(d0, d1);
+      dk[2 * j + 1] = pack_bf16x2(d2, d3);
+    }
+    tmem_st16(tST + ch * 16, pk);  // P^T over S^T columns already read
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int cc = ch * 4 + v;  // 16-byte chunk of the dS^T row: box cc / 8, chunk cc % 8
+      const uint32_t a = ds_row + static_cast<uint32_t>((cc >> 3) * C::BOX_BYTES) +
+                         (static_cast<uint32_t>((cc & 7) ^ (row & 7)) << 4);
+      st_shared_v4(a, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+    }
+  }
 }
 
 // --------------------------------------------------------------------- main
@@ -291,6 +362,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       if (!wait_bar(p_full, it & 1)) break;
       if (leader) {
+        // dQ_i = dS K first (A = dS, the MN-major view of dS^T; B = K MN-major),
+        // into the dP^T columns, so that its drain overlaps the dV and dK products
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_w(tDPT, dsmn_lo + mnmaj(kk), DHI, kmn_lo + mnmaj(kk), DHI, C::IDESC_AB_MN, kk > 0 ? 1u : 0u);
+        mma_commit(dq_full);
         // dV += P^T dO_i (A = P^T from TMEM, B = dO_i MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -300,11 +377,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss_w(tDK, ds_lo + kmaj(kk), DHI, qmn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
-        // dQ_i = dS K (A = dS, the MN-major view of dS^T; B = K MN-major), into the dP^T columns
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss_w(tDPT, dsmn_lo + mnmaj(kk), DHI, kmn_lo + mnmaj(kk), DHI, C::IDESC_AB_MN, kk > 0 ? 1u : 0u);
-        mma_commit(dq_full);
         mma_commit(step_done);
         mma_commit(q_empty + s);
       }
@@ -322,23 +394,32 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int kabs = k0 + row;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tST = tmem + lane_base + C::ST_COL, tDPT = tmem + lane_base + C::DPT_COL;
-    const float sl2 = p.scale_log2;
     bool ok = true;
     const uint32_t ds_row = smem_u32(sDS) + static_cast<uint32_t>(row) * 128u;
+    // this thread's entry of the per-row statistics, loaded one Q tile ahead
+    float nx_lse2 = INFINITY, nx_drow = 0.f;
+    auto fetch = [&](int it) {
+      const int qi = (qt0 + it) * 128 + row;
+      nx_lse2 = INFINITY;
+      nx_drow = 0.f;
+      if (it < n_it && qi < p.Nq) {
+        const size_t gi = static_cast<size_t>(bh) * p.Nq + qi;
+        nx_lse2 = p.lse2[gi];
+        nx_drow = p.drow[gi];
+      }
+    };
+    fetch(0);
     for (int it = 0; ok && it < n_it; ++it) {
       const int q0 = (qt0 + it) * 128;
       ok = mbar_wait(s_full, it & 1, lim, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // this Q tile's lse (log2 units) and D into shared memory; every thread of
-      // the previous step has finished with them (s_full needed all of p_full)
-      {
-        const int qi = q0 + row;
-        const size_t gi = static_cast<size_t>(bh) * p.Nq + qi;
-        s_lse2[row] = qi < p.Nq ? p.lse2[gi] : INFINITY;
-        s_drow[row] = qi < p.Nq ? p.drow[gi] : 0.f;
-      }
+      // stage this Q tile's statistics, negated; every thread of the previous
+      // step has finished with them (s_full needed all of p_full)
+      s_lse2[row] = -nx_lse2;
+      s_drow[row] = -nx_drow;
+      fetch(it + 1);
       mbar_arrive(stat_full);  // release: this thread's two values are visible to the waiters
       ok = mbar_wait(stat_full, it & 1, lim, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
@@ -349,42 +430,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
-      // visible queries of this key row: q >= kabs - delta (causal), q < Nq, kabs < Nk
-      const int q_lo_vis = p.causal ? kabs - delta : INT_MIN;
-      const bool key_ok = kabs < p.Nk;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(tST + ch * 32, sv);
-        tmem_ld32(tDPT + ch * 32, dp);
-        tmem_ld_wait32(sv);
-        reg_fence32(dp);
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pr[2], dsr[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int c = ch * 32 + 2 * i + h;
-            const int qabs = q0 + c;
-            const bool vis = key_ok && qabs >= q_lo_vis && qabs < p.Nq;
-            const float e = ex2_approx(fmaf(u2f(sv[2 * i + h]), sl2, -s_lse2[c]));
-            const float pp = vis ? e : 0.f;
-            pr[h] = pp;
-            dsr[h] = pp * (u2f(dp[2 * i + h]) - s_drow[c]);
-          }
-          pk[i] = pack_bf16x2(pr[0], pr[1]);
-          dk[i] = pack_bf16x2(dsr[0], dsr[1]);
-        }
-        tmem_st16(tST + ch * 16, pk);  // P^T over S^T columns already read
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int cc = ch * 4 + v;  // 16-byte chunk of the dS^T row: box cc / 8, chunk cc % 8
-          const uint32_t a = ds_row + static_cast<uint32_t>((cc >> 3) * C::BOX_BYTES) +
-                             (static_cast<uint32_t>((cc & 7) ^ (row & 7)) << 4);
-          st_shared_v4(a, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
-        }
-      }
+      // Only a Q tile that crosses the causal diagonal (query q sees this key
+      // iff q >= kabs - delta) or a key tile past Nk needs a per-element test.
+      // Key rows >= Nk hold zero K and V (TMA fill) but exp2(0 - lse2) may
+      // overflow there, so they are masked whole; query rows >= Nq carry
+      // lse = +inf, so their weights are 0 without a test.
+      if ((p.causal && k0 + 127 - delta > q0) || k0 + 128 > p.Nk) {
+        const int c_lo = kabs >= p.Nk ? INT_MAX : (p.causal ? kabs - delta - q0 : INT_MIN);
+        sg_tile<D, true>(tST, tDPT, ds_row, row, c_lo, s_lse2, s_drow, p.scale_log2);
+      } else
+        sg_tile<D, false>(tST, tDPT, ds_row, row, 0, s_lse2, s_drow, p.scale_log2);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -438,22 +493,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int qabs = (qt0 + it) * 128 + row;
-      float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qabs) * D;
+      uint32_t a[D];
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t a[32];
-        tmem_ld32(src + ch * 32, a);
-        tmem_ld_wait32(a);
-        if (qabs < p.Nq) {
+      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(src + ch * 32, a + ch * 32);
+      tmem_ld_wait32(a);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            red_add_v4_f32(dst + ch * 32 + 4 * v, u2f(a[4 * v]), u2f(a[4 * v + 1]), u2f(a[4 * v + 2]),
-                           u2f(a[4 * v + 3]));
-        }
-      }
+      for (int ch = 1; ch < D / 32; ++ch) reg_fence32(a + ch * 32);
+      // the dP^T columns may take the next step's dP^T once the loads completed
       tc_fence_before();
       mbar_arrive(dq_free);
+      // Tiled accumulator: one warp's 32 rows of a 4-column chunk are 512
+      // contiguous bytes. Rows past Nq add zeros to the padding.
+      float* dst = p.dq_acc + ((static_cast<size_t>(bh) * nqt + qt0 + it) * (D / 4) * 128 + row) * 4;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 4; ++c4)
+        red_add_v4_f32(dst + c4 * 512, u2f(a[4 * c4]), u2f(a[4 * c4 + 1]), u2f(a[4 * c4 + 2]), u2f(a[4 * c4 + 3]));
     }
   }
 
@@ -469,10 +523,12 @@ template <int D>
 static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout,
                                 const float* lse, void* dq, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
-  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
+  const long long bhc = static_cast<long long>(p.B) * p.H;
+  const long long rows = bhc * p.Nq;
+  const long long rows_pad = bhc * ((p.Nq + 127) / 128) * 128;
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows_pad + 255) / 256), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, p.dq_acc, p.lse2,
-      p.drow, rows);
+      p.drow, bhc, p.Nq);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ctas = static_cast<long long>(p.B) * p.H * ((p.Nk + 127) / 128);
@@ -480,7 +536,7 @@ static cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long n8 = rows * D / 8;
   fa_bwd_finish_kernel<D><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
-      p.dq_acc, static_cast<__nv_bfloat16*>(dq), p.scale, n8);
+      p.dq_acc, static_cast<__nv_bfloat16*>(dq), p.scale, n8, p.Nq);
   return cudaGetLastError();
 }
 

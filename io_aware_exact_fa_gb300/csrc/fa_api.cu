@@ -278,7 +278,8 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int d) {
   if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128)) return 0;
   const size_t rows = static_cast<size_t>(B) * H * Nq;
-  const size_t acc = (rows * d * 4 + 255) & ~size_t(255);
+  const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(Nq) + 127) / 128) * 128;
+  const size_t acc = (rows_pad * d * 4 + 255) & ~size_t(255);
   const size_t stat = (rows * 4 + 255) & ~size_t(255);
   return acc + 2 * stat;
 }
@@ -313,7 +314,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (fa_status s = encode_map(&tv, v, Nk, static_cast<int>(BH), d)) return s;
   if (fa_status s = encode_map(&tdo, dout, Nq, static_cast<int>(BH), d)) return s;
   const size_t rows = static_cast<size_t>(BH) * Nq;
-  const size_t acc = (rows * d * 4 + 255) & ~size_t(255);
+  const size_t rows_pad = static_cast<size_t>(BH) * ((static_cast<size_t>(Nq) + 127) / 128) * 128;
+  const size_t acc = (rows_pad * d * 4 + 255) & ~size_t(255);
   const size_t stat = (rows * 4 + 255) & ~size_t(255);
   fa::BwdParams p{};
   p.dq_acc = static_cast<float*>(workspace);

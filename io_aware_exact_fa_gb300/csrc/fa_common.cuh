@@ -67,7 +67,9 @@ struct PrefillParams {
 };
 
 struct BwdParams {
-  float* dq_acc;             // fp32 [B*H, Nq, d] workspace: dQ / scale, accumulated
+  float* dq_acc;             // fp32 workspace: dQ / scale, accumulated, tiled as
+                             // [B*H][ceil(Nq/128)][d/4][128 rows][4] (one 4-column
+                             // chunk of a 128-row Q tile is 2 KB contiguous)
   float* lse2;               // fp32 [B*H, Nq] workspace: lse * log2(e) (+inf for an empty row)
   float* drow;               // fp32 [B*H, Nq] workspace: sum_c dO * O per row
   void* dk;                  // bf16 [B*H, Nk, d]
