@@ -18,16 +18,19 @@
 //                           vector atomics.
 //   fa_bwd_finish_kernel    dQ = bf16(scale * accumulator).
 //
-// fa_bwd_kernel, 384 threads:
-//   warp 0      TMA producer: K and V once, then Q_i / dO_i into two stages.
-//   warp 1      TMEM allocator and MMA issuer.
-//   warps 4-7   "softmax-grad": each thread owns one key row (TMEM lane) of
-//               S^T = K Q_i^T and dP^T = V dO_i^T, forms P^T and dS^T, writes
-//               P^T (bf16) into the S^T columns and dS^T (bf16) into shared
-//               memory; at the end writes dK and dV.
-//   warps 8-11  dQ drain: each thread owns one query row of dQ_i = dS K.
-// TMEM columns: S^T [0,128) (P^T bf16 in [0,64)), dP^T [128,256) (later
-// dQ_i), dV [256,256+D), dK [256+D,256+2D).
+// fa_bwd_kernel, 512 threads:
+//   warp 0       TMA producer: K and V once, then Q_i / dO_i into two stages.
+//   warp 1       TMEM allocator and MMA issuer.
+//   warps 4-11   "softmax-grad": a thread owns one key row (TMEM lane) and one
+//                half of the 128 query columns of S^T = K Q_i^T and
+//                dP^T = V dO_i^T, forms P^T and dS^T, writes P^T (bf16) into
+//                the S^T columns and dS^T (bf16) into shared memory; at the
+//                end one half writes dV, the other dK.
+//   warps 12-15  dQ drain: a thread owns one query row of dQ_i = dS K.
+// Per step the MMAs run dQ_i, dV_i, S^T_{i+1}, dP^T_{i+1}, dK_i, so the next
+// step's softmax-grad overlaps dK_i and the drain overlaps the rest.
+// TMEM columns: S^T [0,128) (P^T bf16 in [0,32) and [64,96)), dP^T
+// [128,256) (later dQ_i), dV [256,256+D), dK [256+D,256+2D).
 #include <cuda_bf16.h>
 
 #include "fa_ptx.cuh"
@@ -36,11 +39,12 @@ namespace fa {
 
 namespace {
 
-constexpr int BWD_THREADS = 384;
+constexpr int BWD_THREADS = 512;
 constexpr int BWD_TMA_WARP = 0;
 constexpr int BWD_MMA_WARP = 1;
-constexpr int BWD_SG_WARP0 = 4;  // warps 4-7
-constexpr int BWD_DQ_WARP0 = 8;  // warps 8-11
+constexpr int BWD_SG_WARP0 = 4;  // warps 4-11
+constexpr int BWD_SG_THREADS = 256;
+constexpr int BWD_DQ_WARP0 = 12;  // warps 12-15
 
 template <int D>
 struct BwdCfg {
@@ -152,19 +156,23 @@ __global__ void __launch_bounds__(256) fa_bwd_finish_kernel(const float* __restr
   reinterpret_cast<uint4*>(dq)[i] = w;
 }
 
-// --------------------------------------------------------- softmax-grad tile
-// One thread, one key row of a 128 x 128 step: P^T = exp2(S^T * scale * log2(e)
-// - lse2) and dS^T = P^T * (dP^T - D) for the 128 queries of the Q tile. P^T
-// (bf16) goes over the S^T columns already read, dS^T (bf16) into the
-// 128-byte-swizzled shared tile (two 64-column boxes). nlse2 and ndrow hold
-// -lse2 and -D per query column. With MASK, columns below c_lo are masked.
-template <int D, bool MASK>
-__device__ __forceinline__ void sg_tile(uint32_t tST, uint32_t tDPT, uint32_t ds_row, int row, int c_lo,
-                                        const float* nlse2, const float* ndrow, float sl2) {
+// ----------------------------------------------------- softmax-grad half tile
+// One thread, one key row, one half (64 query columns, chunks 2h and 2h + 1) of
+// a 128 x 128 step: P^T = exp2(S^T * scale * log2(e) - lse2) and
+// dS^T = P^T * (dP^T - D). P^T (bf16) goes over S^T columns [64h, 64h + 32),
+// dS^T (bf16) into the 128-byte-swizzled shared tile (box h). nlse2 and ndrow
+// hold -lse2 and -D per query column. With MASK, columns below c_lo are
+// masked. One exponential pair in four runs on the FMA pipe (exp2_fma2) to
+// offload the MUFU unit. before_store() is called once, before the first
+// shared-memory store; if it returns false nothing is stored.
+template <int D, bool MASK, typename F>
+__device__ __forceinline__ bool sg_half(uint32_t tST, uint32_t tDPT, uint32_t ds_row, int row, int h, int c_lo,
+                                        const float* nlse2, const float* ndrow, float sl2, F&& before_store) {
   using C = BwdCfg<D>;
   const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
+  for (int cc = 0; cc < 2; ++cc) {
+    const int ch = 2 * h + cc;
     uint32_t sv[32], dp[32];
     tmem_ld32(tST + ch * 32, sv);
     tmem_ld32(tDPT + ch * 32, dp);
@@ -178,10 +186,18 @@ __device__ __forceinline__ void sg_tile(uint32_t tST, uint32_t tDPT, uint32_t ds
       const float4 nd = *reinterpret_cast<const float4*>(ndrow + c);
       const uint64_t a01 = ffma2(f2pack(u2f(sv[4 * j]), u2f(sv[4 * j + 1])), sl2x2, f2pack(nl.x, nl.y));
       const uint64_t a23 = ffma2(f2pack(u2f(sv[4 * j + 2]), u2f(sv[4 * j + 3])), sl2x2, f2pack(nl.z, nl.w));
-      float x0, x1, x2, x3;
+      float x0, x1, p0, p1, p2, p3;
       f2unpack(a01, x0, x1);
-      f2unpack(a23, x2, x3);
-      float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+      p0 = ex2_approx(x0);
+      p1 = ex2_approx(x1);
+      if (j & 1) {
+        f2unpack(exp2_fma2(a23), p2, p3);
+      } else {
+        float x2, x3;
+        f2unpack(a23, x2, x3);
+        p2 = ex2_approx(x2);
+        p3 = ex2_approx(x3);
+      }
       if (MASK) {
         p0 = c >= c_lo ? p0 : 0.f;
         p1 = c + 1 >= c_lo ? p1 : 0.f;
@@ -198,15 +214,19 @@ __device__ __forceinline__ void sg_tile(uint32_t tST, uint32_t tDPT, uint32_t ds
       dk[2 * j] = pack_bf16x2(d0, d1);
       dk[2 * j + 1] = pack_bf16x2(d2, d3);
     }
-    tmem_st16(tST + ch * 16, pk);  // P^T over S^T columns already read
+    // P^T over S^T columns this thread already read: half h keeps its 64
+    // queries (32 bf16x2 columns) at column 64 h, inside its own S^T columns
+    tmem_st16(tST + h * 64 + cc * 16, pk);
+    if (cc == 0 && !before_store()) return false;
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      const int cc = ch * 4 + v;  // 16-byte chunk of the dS^T row: box cc / 8, chunk cc % 8
-      const uint32_t a = ds_row + static_cast<uint32_t>((cc >> 3) * C::BOX_BYTES) +
-                         (static_cast<uint32_t>((cc & 7) ^ (row & 7)) << 4);
+      // 16-byte chunk (ch % 2) * 4 + v of the row's 128-byte line in box h
+      const uint32_t a = ds_row + static_cast<uint32_t>(h * C::BOX_BYTES) +
+                         (static_cast<uint32_t>(((cc * 4 + v) ^ (row & 7))) << 4);
       st_shared_v4(a, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
     }
   }
+  return true;
 }
 
 // --------------------------------------------------------------------- main
@@ -222,20 +242,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint8_t* sV = smem + C::V_OFF;
   uint8_t* sQ0 = smem + C::Q_OFF;  // stage s: Q at Q_OFF + s*2*TILE, dO right after
   uint8_t* sDS = smem + C::DS_OFF;
-  float* s_lse2 = reinterpret_cast<float*>(smem + C::STAT_OFF);
-  float* s_drow = s_lse2 + 128;
+  float* s_nlse2 = reinterpret_cast<float*>(smem + C::STAT_OFF);  // -lse2 per query of the step
+  float* s_ndrow = s_nlse2 + 128;                                  // -D per query of the step
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;     // [2]
   uint64_t* q_empty = bars + 3;    // [2]
   uint64_t* s_full = bars + 5;     // S^T and dP^T of a step computed
-  uint64_t* p_full = bars + 6;     // P^T stored in TMEM and dS^T in shared memory
+  uint64_t* p_full = bars + 6;     // P^T stored in TMEM and dS^T in shared memory (all softmax-grad threads)
   uint64_t* dv_done = bars + 7;    // the step's dV MMA (reading P^T from the S^T columns) completed
-  uint64_t* step_done = bars + 8;  // every MMA of the step completed (dS^T may be rewritten)
+  uint64_t* step_done = bars + 8;  // the step's last MMA (dK) completed: dS^T may be rewritten
   uint64_t* dq_full = bars + 9;    // dQ_i in the dP^T columns
   uint64_t* dq_free = bars + 10;   // dQ_i read out
   uint64_t* acc_done = bars + 11;  // every MMA completed: dK, dV final
-  uint64_t* stat_full = bars + 12; // the step's lse / D staged in shared memory by all 128 threads
+  uint64_t* stat_full = bars + 12; // the step's lse / D staged in shared memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -258,13 +278,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(q_empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, BWD_SG_THREADS);
     mbar_init(dv_done, 1);
     mbar_init(step_done, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
     mbar_init(acc_done, 1);
-    mbar_init(stat_full, 128);
+    mbar_init(stat_full, BWD_SG_THREADS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -319,6 +339,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     __syncwarp();
   } else if (warp == BWD_MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
+    // Per step i: dQ_i, dV_i, then (for step i + 1) S^T and dP^T, then dK_i,
+    // so the next step's softmax-grad starts while dK_i runs.
     const bool leader = lane == 0;
     bool ok = true;
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
@@ -337,48 +359,59 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // MN-major K-step kk: 16 rows = 2048 bytes in (64-column boxes LBO apart)
     auto kmaj = [](int kk) { return static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
     auto mnmaj = [](int kk) { return static_cast<uint32_t>((kk * 2048) >> 4); };
-    if (n_it > 0 && !wait_bar(kv_full, 0)) ok = false;
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int s = it & 1;
-      const uint32_t q_base = smem_u32(sQ0) + s * 2 * C::TILE_BYTES;
-      const uint32_t q_lo = sdesc_sw128_lo(q_base, 16), qmn_lo = sdesc_sw128_lo(q_base, C::BOX_BYTES);
-      const uint32_t do_lo = sdesc_sw128_lo(q_base + C::TILE_BYTES, 16),
-                     domn_lo = sdesc_sw128_lo(q_base + C::TILE_BYTES, C::BOX_BYTES);
-      if (!wait_bar(q_full + s, (it >> 1) & 1)) break;
-      // S^T (the S^T columns) is rewritten only after the previous dV read P^T there
-      if (it > 0 && !wait_bar(dv_done, (it - 1) & 1)) break;
+    auto stage = [&](int it) { return smem_u32(sQ0) + (it & 1) * 2 * C::TILE_BYTES; };
+    // S^T = K Q_i^T and dP^T = V dO_i^T of step it (both operands K-major)
+    auto issue_s_dp = [&](int it) {
+      const uint32_t qb = stage(it);
+      const uint32_t q_lo = sdesc_sw128_lo(qb, 16), do_lo = sdesc_sw128_lo(qb + C::TILE_BYTES, 16);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_w(tST, k_lo + kmaj(kk), DHI, q_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
       }
       // dP^T (the dP^T columns) only after the previous dQ_i was read out
-      if (it > 0 && !wait_bar(dq_free, (it - 1) & 1)) break;
+      if (it > 0 && !wait_bar(dq_free, (it - 1) & 1)) return false;
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_w(tDPT, v_lo + kmaj(kk), DHI, do_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
         mma_commit(s_full);
       }
+      return true;
+    };
+    if (n_it > 0) {
+      if (wait_bar(kv_full, 0) && wait_bar(q_full, 0)) issue_s_dp(0);
+    }
+    for (int it = 0; ok && it < n_it; ++it) {
+      const uint32_t qb = stage(it);
+      const uint32_t qmn_lo = sdesc_sw128_lo(qb, C::BOX_BYTES), domn_lo = sdesc_sw128_lo(qb + C::TILE_BYTES, C::BOX_BYTES);
       if (!wait_bar(p_full, it & 1)) break;
       if (leader) {
-        // dQ_i = dS K first (A = dS, the MN-major view of dS^T; B = K MN-major),
-        // into the dP^T columns, so that its drain overlaps the dV and dK products
+        // dQ_i = dS K (A = dS, the MN-major view of dS^T; B = K MN-major), into the dP^T columns
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss_w(tDPT, dsmn_lo + mnmaj(kk), DHI, kmn_lo + mnmaj(kk), DHI, C::IDESC_AB_MN, kk > 0 ? 1u : 0u);
         mma_commit(dq_full);
-        // dV += P^T dO_i (A = P^T from TMEM, B = dO_i MN-major)
+        // dV += P^T dO_i (A = P^T from TMEM: queries 16kk.. at column 8kk
+        // for the first half, 64 + 8(kk - 4) for the second; B = dO_i MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts_w(tDV, tST + kk * 8, domn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tDV, tST + kk * 8 + (kk >= 4 ? 32 : 0), domn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(dv_done);
+      }
+      if (it + 1 < n_it) {
+        // the next S^T overwrites P^T_i: only after dV_i read it
+        if (!wait_bar(q_full + ((it + 1) & 1), ((it + 1) >> 1) & 1)) break;
+        if (!wait_bar(dv_done, it & 1)) break;
+        if (!issue_s_dp(it + 1)) break;
+      }
+      if (leader) {
         // dK += dS^T Q_i (A = dS^T K-major, B = Q_i MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss_w(tDK, ds_lo + kmaj(kk), DHI, qmn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(step_done);
-        mma_commit(q_empty + s);
+        mma_commit(q_empty + (it & 1));
       }
     }
     if (leader) {
@@ -387,26 +420,27 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_drain(acc_done, 0, lim);  // every MMA completed before TMEM is released
     }
     __syncwarp();
-  } else if (warp >= BWD_SG_WARP0 && warp < BWD_SG_WARP0 + 4) {
+  } else if (warp >= BWD_SG_WARP0 && warp < BWD_DQ_WARP0) {
     // ---------------------------------------------------------- softmax-grad
-    const int wq = warp - BWD_SG_WARP0;
+    // warp w: key rows 32 * (w % 4) .. + 31 (its TMEM lane quarter), query
+    // columns 64 * h .. + 63 with h = (w - 4) / 4
+    const int wq = warp & 3;
+    const int h = (warp - BWD_SG_WARP0) >> 2;
     const int row = wq * 32 + lane;  // key row within the tile
     const int kabs = k0 + row;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tST = tmem + lane_base + C::ST_COL, tDPT = tmem + lane_base + C::DPT_COL;
     bool ok = true;
     const uint32_t ds_row = smem_u32(sDS) + static_cast<uint32_t>(row) * 128u;
-    // this thread's entry of the per-row statistics, loaded one Q tile ahead
-    float nx_lse2 = INFINITY, nx_drow = 0.f;
+    // one entry of the per-row statistics (h = 0: lse2, h = 1: D) of query
+    // row `row` of the Q tile, loaded one step ahead
+    const float* stat_src = h ? p.drow : p.lse2;
+    float* stat_dst = (h ? s_ndrow : s_nlse2) + row;
+    float nx = 0.f;
     auto fetch = [&](int it) {
       const int qi = (qt0 + it) * 128 + row;
-      nx_lse2 = INFINITY;
-      nx_drow = 0.f;
-      if (it < n_it && qi < p.Nq) {
-        const size_t gi = static_cast<size_t>(bh) * p.Nq + qi;
-        nx_lse2 = p.lse2[gi];
-        nx_drow = p.drow[gi];
-      }
+      nx = h ? 0.f : INFINITY;
+      if (it < n_it && qi < p.Nq) nx = stat_src[static_cast<size_t>(bh) * p.Nq + qi];
     };
     fetch(0);
     for (int it = 0; ok && it < n_it; ++it) {
@@ -417,19 +451,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc_fence_after();
       // stage this Q tile's statistics, negated; every thread of the previous
       // step has finished with them (s_full needed all of p_full)
-      s_lse2[row] = -nx_lse2;
-      s_drow[row] = -nx_drow;
+      *stat_dst = -nx;
       fetch(it + 1);
-      mbar_arrive(stat_full);  // release: this thread's two values are visible to the waiters
+      mbar_arrive(stat_full);  // release: this thread's value is visible to the waiters
       ok = mbar_wait(stat_full, it & 1, lim, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      // dS^T in shared memory is rewritten only after the previous step's dK and dQ read it
-      if (it > 0) {
-        ok = mbar_wait(step_done, (it - 1) & 1, lim, p.status, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-      }
+      // dS^T in shared memory is rewritten only after the previous step's dK
+      // (its last reader) completed
+      auto before_store = [&]() {
+        if (it == 0) return true;
+        bool w = mbar_wait(step_done, (it - 1) & 1, lim, p.status, abort_flag);
+        return __all_sync(0xffffffffu, w) != 0;
+      };
       // Only a Q tile that crosses the causal diagonal (query q sees this key
       // iff q >= kabs - delta) or a key tile past Nk needs a per-element test.
       // Key rows >= Nk hold zero K and V (TMA fill) but exp2(0 - lse2) may
@@ -437,15 +471,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // lse = +inf, so their weights are 0 without a test.
       if ((p.causal && k0 + 127 - delta > q0) || k0 + 128 > p.Nk) {
         const int c_lo = kabs >= p.Nk ? INT_MAX : (p.causal ? kabs - delta - q0 : INT_MIN);
-        sg_tile<D, true>(tST, tDPT, ds_row, row, c_lo, s_lse2, s_drow, p.scale_log2);
-      } else
-        sg_tile<D, false>(tST, tDPT, ds_row, row, 0, s_lse2, s_drow, p.scale_log2);
+        ok = sg_half<D, true>(tST, tDPT, ds_row, row, h, c_lo, s_nlse2, s_ndrow, p.scale_log2, before_store);
+      } else {
+        ok = sg_half<D, false>(tST, tDPT, ds_row, row, h, 0, s_nlse2, s_ndrow, p.scale_log2, before_store);
+      }
+      if (!ok) break;
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full);
     }
-    // ---- epilogue: dK = scale * acc, dV = acc (bf16), rows below Nk
+    // ---- epilogue: h = 0 writes dV = acc, h = 1 writes dK = scale * acc (bf16), rows below Nk
     if (ok) {
       ok = mbar_wait(acc_done, 0, lim, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
@@ -455,36 +491,32 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (ok) {
       const bool row_ok = kabs < p.Nk;
       const size_t kr = static_cast<size_t>(bh) * p.Nk + (row_ok ? kabs : 0);
-      __nv_bfloat16* dvr = reinterpret_cast<__nv_bfloat16*>(p.dv) + kr * D;
-      __nv_bfloat16* dkr = reinterpret_cast<__nv_bfloat16*>(p.dk) + kr * D;
+      const uint32_t src = tmem + lane_base + (h ? C::DK_COL : C::DV_COL);
+      const float f = h ? p.scale : 1.f;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(h ? p.dk : p.dv) + kr * D;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t src = tmem + lane_base + (which ? C::DK_COL : C::DV_COL);
-        const float f = which ? p.scale : 1.f;
-        __nv_bfloat16* dst = which ? dkr : dvr;
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t a[32];
+        if (n_it > 0) {
+          tmem_ld32(src + ch * 32, a);
+          tmem_ld_wait32(a);
+        } else {
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t a[32];
-          if (n_it > 0) {
-            tmem_ld32(src + ch * 32, a);
-            tmem_ld_wait32(a);
-          } else {
+          for (int i = 0; i < 32; ++i) a[i] = 0u;
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = 0u;
-          }
-          uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            if (row_ok) d4[v] = make_uint4(pack_bf16x2(u2f(a[8 * v]) * f, u2f(a[8 * v + 1]) * f),
+        for (int v = 0; v < 4; ++v)
+          if (row_ok)
+            d4[v] = make_uint4(pack_bf16x2(u2f(a[8 * v]) * f, u2f(a[8 * v + 1]) * f),
                                pack_bf16x2(u2f(a[8 * v + 2]) * f, u2f(a[8 * v + 3]) * f),
                                pack_bf16x2(u2f(a[8 * v + 4]) * f, u2f(a[8 * v + 5]) * f),
                                pack_bf16x2(u2f(a[8 * v + 6]) * f, u2f(a[8 * v + 7]) * f));
-        }
       }
     }
   } else if (warp >= BWD_DQ_WARP0) {
     // -------------------------------------------------------------- dQ drain
-    const int wq = warp - BWD_DQ_WARP0;
+    const int wq = warp & 3;
     const int row = wq * 32 + lane;  // query row within the Q tile
     const uint32_t src = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::DPT_COL;
     bool ok = true;
@@ -493,21 +525,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t a[D];
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(src + ch * 32, a + ch * 32);
-      tmem_ld_wait32(a);
-#pragma unroll
-      for (int ch = 1; ch < D / 32; ++ch) reg_fence32(a + ch * 32);
-      // the dP^T columns may take the next step's dP^T once the loads completed
-      tc_fence_before();
-      mbar_arrive(dq_free);
       // Tiled accumulator: one warp's 32 rows of a 4-column chunk are 512
       // contiguous bytes. Rows past Nq add zeros to the padding.
       float* dst = p.dq_acc + ((static_cast<size_t>(bh) * nqt + qt0 + it) * (D / 4) * 128 + row) * 4;
 #pragma unroll
-      for (int c4 = 0; c4 < D / 4; ++c4)
-        red_add_v4_f32(dst + c4 * 512, u2f(a[4 * c4]), u2f(a[4 * c4 + 1]), u2f(a[4 * c4 + 2]), u2f(a[4 * c4 + 3]));
+      for (int hh = 0; hh < D / 32; ++hh) {
+        uint32_t a[32];
+        tmem_ld32(src + hh * 32, a);
+        tmem_ld_wait32(a);
+        if (hh == D / 32 - 1) {
+          // the dP^T columns may take the next step's dP^T once the loads completed
+          tc_fence_before();
+          mbar_arrive(dq_free);
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          red_add_v4_f32(dst + (hh * 8 + c4) * 512, u2f(a[4 * c4]), u2f(a[4 * c4 + 1]), u2f(a[4 * c4 + 2]),
+                         u2f(a[4 * c4 + 3]));
+      }
     }
   }
 
