@@ -163,11 +163,14 @@ __global__ void __launch_bounds__(256) fa_bwd_finish_kernel(const float* __restr
 // dS^T (bf16) into the 128-byte-swizzled shared tile (box h). nlse2 and ndrow
 // hold -lse2 and -D per query column. With MASK, columns below c_lo are
 // masked. One exponential pair in four runs on the FMA pipe (exp2_fma2) to
-// offload the MUFU unit. before_store() is called once, before the first
-// shared-memory store; if it returns false nothing is stored.
-template <int D, bool MASK, typename F>
+// offload the MUFU unit. before_math() is called once, after the first TMEM
+// loads are issued and before the statistics are read; before_store() once,
+// before the first shared-memory store. If either returns false the step
+// stops there.
+template <int D, bool MASK, typename F, typename G>
 __device__ __forceinline__ bool sg_half(uint32_t tST, uint32_t tDPT, uint32_t ds_row, int row, int h, int c_lo,
-                                        const float* nlse2, const float* ndrow, float sl2, F&& before_store) {
+                                        const float* nlse2, const float* ndrow, float sl2, G&& before_math,
+                                        F&& before_store) {
   using C = BwdCfg<D>;
   const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
@@ -176,6 +179,11 @@ __device__ __forceinline__ bool sg_half(uint32_t tST, uint32_t tDPT, uint32_t ds
     uint32_t sv[32], dp[32];
     tmem_ld32(tST + ch * 32, sv);
     tmem_ld32(tDPT + ch * 32, dp);
+    if (cc == 0 && !before_math()) {
+      tmem_ld_wait32(sv);
+      reg_fence32(dp);
+      return false;
+    }
     tmem_ld_wait32(sv);
     reg_fence32(dp);
     uint32_t pk[16], dk[16];
@@ -454,9 +462,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       *stat_dst = -nx;
       fetch(it + 1);
       mbar_arrive(stat_full);  // release: this thread's value is visible to the waiters
-      ok = mbar_wait(stat_full, it & 1, lim, p.status, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      // the statistics are waited for once the first TMEM loads are in flight
+      auto before_math = [&]() {
+        const bool w = mbar_wait(stat_full, it & 1, lim, p.status, abort_flag);
+        return __all_sync(0xffffffffu, w) != 0;
+      };
       // dS^T in shared memory is rewritten only after the previous step's dK
       // (its last reader) completed
       auto before_store = [&]() {
@@ -471,9 +481,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // lse = +inf, so their weights are 0 without a test.
       if ((p.causal && k0 + 127 - delta > q0) || k0 + 128 > p.Nk) {
         const int c_lo = kabs >= p.Nk ? INT_MAX : (p.causal ? kabs - delta - q0 : INT_MIN);
-        ok = sg_half<D, true>(tST, tDPT, ds_row, row, h, c_lo, s_nlse2, s_ndrow, p.scale_log2, before_store);
+        ok = sg_half<D, true>(tST, tDPT, ds_row, row, h, c_lo, s_nlse2, s_ndrow, p.scale_log2, before_math,
+                              before_store);
       } else {
-        ok = sg_half<D, false>(tST, tDPT, ds_row, row, h, 0, s_nlse2, s_ndrow, p.scale_log2, before_store);
+        ok = sg_half<D, false>(tST, tDPT, ds_row, row, h, 0, s_nlse2, s_ndrow, p.scale_log2, before_math,
+                               before_store);
       }
       if (!ok) break;
       tmem_st_wait();
