@@ -135,6 +135,36 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
 fa_status fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                                     int B, int H, int Nk, int d, float scale, int num_splits, void* stream);
 
+/* Bytes of device workspace fa_decode_grouped needs: the split-KV partial
+ * states of B*H*Nq query rows, fa_decode_workspace_size(B, H*Nq, d,
+ * num_splits). Returns 0 for invalid arguments (including Nq > 128). */
+size_t fa_decode_grouped_workspace_size(int B, int H, int Nq, int d, int num_splits);
+
+/* Split-KV decode with grouped K/V heads, several new query tokens per
+ * sequence and per-sequence KV lengths (the decode variants next to
+ * "FlashAttention: Attention Is Limited by Memory, Not Math", section "Where
+ * it helps, and where it does not"; the merge as for fa_decode_splitkv).
+ * H query heads share Hkv K/V heads: query head h reads K/V head h / (H/Hkv).
+ * Sequence b holds L_b = seqlens_k[b] keys (clamped to [0, Nk]; all Nk when
+ * seqlens_k is NULL), and its Nq new tokens are its last Nq positions: token t
+ * sees key j iff j < L_b and j <= L_b - Nq + t. A token that sees no key gets
+ * o = 0 and lse = -inf. The (H/Hkv)*Nq query rows of one (b, K/V head) form
+ * one tensor-core tile, so each K/V byte is read once per group.
+ *   q, o       bf16 [B, H, Nq, d]      k_cache, v_cache  bf16 [B, Hkv, Nk, d]
+ *   seqlens_k  int32 [B] in device memory, or NULL
+ *   lse        fp32 [B, H, Nq] (may be NULL)
+ *   workspace  device memory of at least fa_decode_grouped_workspace_size()
+ *              bytes, 256-byte aligned, owned by the caller; overwritten.
+ *   Split s covers keys [s*c, min(L_b, (s+1)*c)), c = ceil(Nk / num_splits)
+ *   rounded up to a multiple of 128; 1 <= num_splits <= 1024.
+ * Errors: FA_ERR_INVALID_ARG for NULL tensors, sizes < 1, H not a multiple of
+ * Hkv or a bad scale; FA_ERR_UNSUPPORTED for d not in {64, 128},
+ * (H/Hkv)*Nq > 128 or misaligned pointers; FA_ERR_WORKSPACE. Two launches
+ * (grouped split kernel, then merge) on `stream`. */
+fa_status fa_decode_grouped(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,
+                            float* lse, int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator of
  * B*H*ceil(Nq/128)*128*d elements (Nq padded to whole 128-row tiles) and two
  * fp32 per-row statistics [B, H, Nq], each rounded up to 256 bytes. Returns 0

@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfa_gb300.so")
-SOURCES = ["fa_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "backward_sm103.cu"]
+SOURCES = ["fa_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "backward_sm103.cu", "decode_grouped_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

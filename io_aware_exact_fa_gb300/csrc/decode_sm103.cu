@@ -209,6 +209,16 @@ cudaError_t launch_decode(int d, const DecodeParams& p, cudaStream_t stream) {
   return d == 64 ? launch_decode_t<64>(p, stream) : launch_decode_t<128>(p, stream);
 }
 
+// The merge pass alone, over p.BH rows of p.S partial states each (used by the
+// grouped decode, whose rows are the B * H * Nq query tokens).
+cudaError_t launch_decode_merge(int d, const DecodeParams& p, cudaStream_t stream) {
+  if (d == 64)
+    fa_decode_merge_kernel<64><<<p.BH, 64, 0, stream>>>(p);
+  else
+    fa_decode_merge_kernel<128><<<p.BH, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 // Self-test of the bounded wait: one warp waits on an mbarrier that nothing
 // ever arrives on; the wait gives up after limit_ns and records FA_DEV_TIMEOUT.
 __global__ void fa_wait_selftest_kernel(uint64_t limit_ns, unsigned int* status) {

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "decode_grouped.cuh"
 #include "fa_common.cuh"
 
 #ifndef FA_TAIL_SPLIT
@@ -81,6 +82,10 @@ fa_status device_state(DeviceState** out) {
     if ((e = fa::prefill_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
     if ((e = fa::bwd_set_attributes(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=64)");
     if ((e = fa::bwd_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=128)");
+    if ((e = fa::decode_grouped_set_attributes(64)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(grouped decode d=64)");
+    if ((e = fa::decode_grouped_set_attributes(128)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(grouped decode d=128)");
     // The in-kernel register split assumes this launch allocation; a
     // different one could make setmaxnreg.inc wait forever, so refuse.
     for (int d : {64, 128}) {
@@ -271,6 +276,78 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
   p.scale_log2 = scale * 1.4426950408889634f;
   cudaError_t e = fa::launch_decode(d, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  t_launches += 2;
+  return FA_OK;
+}
+
+size_t fa_decode_grouped_workspace_size(int B, int H, int Nq, int d, int num_splits) {
+  if (Nq < 1 || Nq > 128 || static_cast<long long>(H) * Nq > INT_MAX) return 0;
+  return fa_decode_workspace_size(B, H * Nq, d, num_splits);
+}
+
+fa_status fa_decode_grouped(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,
+                            float* lse, int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  t_detail[0] = 0;
+  if (!q || !k_cache || !v_cache || !o) return fail(FA_ERR_INVALID_ARG, "q, k_cache, v_cache and o must be non-NULL");
+  if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < 1)
+    return fail(FA_ERR_INVALID_ARG, "need B, H, Hkv, Nq, Nk >= 1 (got %d %d %d %d %d)", B, H, Hkv, Nq, Nk);
+  if (H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H (%d) must be a multiple of Hkv (%d)", H, Hkv);
+  if (num_splits < 1 || num_splits > 1024) return fail(FA_ERR_INVALID_ARG, "num_splits must be in [1, 1024]");
+  if (fa_status s = check_scale(scale)) return s;
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
+  const int G = H / Hkv;
+  if (static_cast<long long>(G) * Nq > 128)
+    return fail(FA_ERR_UNSUPPORTED, "(H / Hkv) * Nq = %lld query rows per K/V head; at most 128",
+                static_cast<long long>(G) * Nq);
+  const long long rows = static_cast<long long>(B) * H * Nq;
+  if (static_cast<long long>(B) * Hkv * num_splits > INT_MAX || rows * num_splits > INT_MAX)
+    return fail(FA_ERR_INVALID_ARG, "B * H * Nq * num_splits is too large");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16))
+    return fail(FA_ERR_UNSUPPORTED, "q, k_cache, v_cache, o must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(FA_ERR_UNSUPPORTED, "lse must be 4-byte aligned");
+  if (seqlens_k && !aligned(seqlens_k, 4)) return fail(FA_ERR_UNSUPPORTED, "seqlens_k must be 4-byte aligned");
+  const size_t need = fa_decode_grouped_workspace_size(B, H, Nq, d, num_splits);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", need);
+
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  const int BHkv = B * Hkv;
+  CUtensorMap tq, tk, tv;
+  if (fa_status s = encode_map(&tq, q, G * Nq, BHkv, d)) return s;  // the G*Nq rows of a group are contiguous
+  if (fa_status s = encode_map(&tk, k_cache, Nk, BHkv, d)) return s;
+  if (fa_status s = encode_map(&tv, v_cache, Nk, BHkv, d)) return s;
+  const size_t parts = static_cast<size_t>(rows) * num_splits;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((parts * d * 4 + 255) & ~size_t(255)));
+  fa::DecodeGroupedParams p{};
+  p.seqlens = seqlens_k;
+  p.ws_o = ws_o;
+  p.ws_ml = ws_ml;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.Nq = Nq;
+  p.R = G * Nq;
+  p.Nk = Nk;
+  p.S = num_splits;
+  p.chunk = ((Nk + num_splits - 1) / num_splits + 127) / 128 * 128;
+  p.scale_log2 = fmaxf(scale * 1.4426950408889634f, 1.17549435e-38f);
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.status = st->status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_decode_grouped(d, tq, tk, tv, p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "grouped decode launch");
+  fa::DecodeParams m{};
+  m.o = o;
+  m.lse = lse;
+  m.ws_o = ws_o;
+  m.ws_ml = ws_ml;
+  m.BH = static_cast<int>(rows);
+  m.S = num_splits;
+  if ((e = fa::launch_decode_merge(d, m, s)) != cudaSuccess) return cuda_fail(e, "grouped decode merge launch");
   t_launches += 2;
   return FA_OK;
 }

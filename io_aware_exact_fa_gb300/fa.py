@@ -40,6 +40,8 @@ EXPORTS = {
     "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_decode_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_decode_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "fa_decode_grouped_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "fa_decode_grouped": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
@@ -156,6 +158,47 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, scale:
                                 int(num_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                 _stream_ptr(stream))
     _check(rc, "fa_decode_splitkv")
+    return out, lse
+
+
+def decode_grouped_workspace_size(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
+    return int(_lib.fa_decode_grouped_workspace_size(B, H, Nq, d, num_splits))
+
+
+def decode_grouped(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   seqlens_k: Optional[torch.Tensor] = None, scale: Optional[float] = None, num_splits: int = 8,
+                   workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, with_lse: bool = True,
+                   stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Decode with grouped K/V heads, Nq new tokens and per-sequence lengths (fa.h fa_decode_grouped):
+    q [B,H,Nq,d], caches [B,Hkv,Nk,d] bf16, seqlens_k int32 [B] or None -> (o [B,H,Nq,d], lse [B,H,Nq])."""
+    _need(q, "q"); _need(k_cache, "k_cache"); _need(v_cache, "v_cache")
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Hkv, Nk, d) or v_cache.shape != (B, Hkv, Nk, d):
+        raise ValueError("k_cache and v_cache must be [B, Hkv, Nk, d]")
+    if seqlens_k is not None:
+        _need(seqlens_k, "seqlens_k", torch.int32)
+        if seqlens_k.shape != (B,):
+            raise ValueError("seqlens_k must be int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = decode_grouped_workspace_size(B, H, Nq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out")
+    if with_lse and lse is None:
+        lse = torch.empty(B, H, Nq, dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    rc = _lib.fa_decode_grouped(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                seqlens_k.data_ptr() if seqlens_k is not None else None, out.data_ptr(),
+                                lse.data_ptr() if lse is not None else None, B, H, Hkv, Nq, Nk, d, float(scale),
+                                int(num_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_ptr(stream))
+    _check(rc, "fa_decode_grouped")
     return out, lse
 
 

@@ -67,6 +67,51 @@ WORKLOADS = {
                           1.0 / math.sqrt(128.0), (False,), kind="decode", num_splits=16),
 }
 
+@dataclasses.dataclass(frozen=True)
+class DecodeVariant:
+    """Decode with grouped K/V heads, Nq new tokens per sequence and ragged
+    per-sequence KV lengths drawn uniformly from [len_lo, Nk] (seeded)."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    scale: float
+    num_splits: int
+    len_lo: int
+
+    def io_bytes(self, seqlens: Sequence[int]) -> int:
+        """Minimum HBM bytes: the visible K and V rows of every sequence read
+        once, q and o (2-byte elements) and the fp32 lse."""
+        kv = 2 * self.Hkv * self.d * 2 * int(sum(min(max(int(x), 0), self.Nk) for x in seqlens))
+        qo = 2 * self.B * self.H * self.Nq * self.d * 2
+        return kv + qo + 4 * self.B * self.H * self.Nq
+
+
+DECODE_VARIANTS = {
+    # 4 query heads per K/V head, one new token, ragged lengths in [4096, 8192]
+    "gqa": DecodeVariant("decode_gqa_b64h32kv8nq1_nk8192d128_ragged", 64, 32, 8, 1, 8192, 128,
+                         1.0 / math.sqrt(128.0), 4, 4096),
+    # the same with 4 new (speculative) tokens per sequence
+    "gqa_spec": DecodeVariant("decode_gqa_b64h32kv8nq4_nk8192d128_ragged", 64, 32, 8, 4, 8192, 128,
+                              1.0 / math.sqrt(128.0), 4, 4096),
+}
+
+
+def make_decode_inputs(w: DecodeVariant, seed: int = 0, device: str = "cpu"):
+    """q [B,H,Nq,d], k/v [B,Hkv,Nk,d] bf16 (order q, k, v) and seqlens int32 [B]
+    uniform in [len_lo, Nk], drawn after v from the same generator."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q = torch.randn(w.B, w.H, w.Nq, w.d, generator=g, device=device, dtype=torch.float32)
+    k = torch.randn(w.B, w.Hkv, w.Nk, w.d, generator=g, device=device, dtype=torch.float32)
+    v = torch.randn(w.B, w.Hkv, w.Nk, w.d, generator=g, device=device, dtype=torch.float32)
+    lens = torch.randint(w.len_lo, w.Nk + 1, (w.B,), generator=g, device=device, dtype=torch.int32)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), lens
+
+
 PR1_OFFSET_ROWS = (124, 125, 126, 127)
 PR1_OFFSET_SIGNS = (+1.0, -1.0, +1.0, -1.0)
 PR1_OFFSET = 1.0e3
