@@ -66,11 +66,15 @@ def visible_pair_fraction(wp, causal: bool) -> float:
     return (wp.pad_heads * padded + (wp.H - wp.pad_heads) * full) / (wp.H * full)
 
 
+# headers a kernel source includes besides fa_ptx.cuh and fa_common.cuh
+KERNEL_HEADERS = {"decode_grouped_sm103.cu": ("decode_grouped.cuh",)}
+
+
 def kernel_hash(name: str) -> str:
-    src = os.path.join(ROOT, "io_aware_exact_fa_gb300", "csrc", name)
+    csrc = os.path.join(ROOT, "io_aware_exact_fa_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (src, os.path.join(ROOT, "io_aware_exact_fa_gb300", "csrc", "fa_ptx.cuh"),
-              os.path.join(ROOT, "io_aware_exact_fa_gb300", "csrc", "fa_common.cuh")):
+    for f in (os.path.join(csrc, name), os.path.join(csrc, "fa_ptx.cuh"), os.path.join(csrc, "fa_common.cuh"),
+              *(os.path.join(csrc, x) for x in KERNEL_HEADERS.get(name, ()))):
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
@@ -255,6 +259,73 @@ def run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, worl
     return out
 
 
+def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
+    """Time fa_decode_grouped on each decode-variant workload (grouped K/V
+    heads, ragged lengths, 1 or 4 new tokens). Inputs are drawn on the device
+    with the workload recipe; the K/V caches (2 GB) exceed L2, so no flush."""
+    import torch
+    import torch.distributed as dist
+    peaks = measured_peaks()
+    out = {"workloads": {}}
+    t_first = None
+    for key, w in W.DECODE_VARIANTS.items():
+        q, k, v, lens = W.make_decode_inputs(w, seed=3000 + rank, device="cuda")
+        ws = torch.empty(fa.decode_grouped_workspace_size(w.B, w.H, w.Nq, w.d, w.num_splits), dtype=torch.uint8,
+                         device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device=dev)
+
+        def call():
+            fa.decode_grouped(q, k, v, seqlens_k=lens, scale=w.scale, num_splits=w.num_splits, workspace=ws,
+                              out=o, lse=lse)
+
+        for _ in range(warm):
+            call()
+        torch.cuda.synchronize()
+        if fa.device_status() != fa.FA_OK:
+            raise RuntimeError("device status not OK after the decode-variant warm-up")
+        K = args.steps
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        t_first = t_first or t0
+        n0 = fa.launch_count()
+        ev[0].record(stream)
+        for i in range(K):
+            call()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        launches = fa.launch_count() - n0
+        if fa.device_status() != fa.FA_OK:
+            raise RuntimeError("device status not OK after the decode-variant timed region")
+        tt = torch.tensor([ev[0].elapsed_time(ev[K]) / 1e3], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = tt.item()
+        nbytes = w.io_bytes(lens.tolist())
+        ach = K * nbytes / t / 1e9
+        out["workloads"][w.name] = {
+            "value": world * ach, "unit": "GB/s", "ms": t / K * 1e3, "bytes": nbytes, "gpu_launches": launches,
+            "config": {"B": w.B, "H": w.H, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "num_splits": w.num_splits, "seqlens": f"uniform in [{w.len_lo}, {w.Nk}], seeded",
+                       "mean_seqlen": float(lens.float().mean().item())},
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"],
+                         "traffic": recorded_traffic("decode_grouped_sm103.cu", w.name),
+                         "kernel": f"fa_decode_grouped_kernel<{w.d}> + fa_decode_merge_kernel<{w.d}>",
+                         "peak_source": f"{peaks['source']} copy",
+                         "bytes_convention": "visible K and V rows read once, q and o written, lse"},
+        }
+        del q, k, v, ws, o, lse
+        torch.cuda.empty_cache()
+    out["_window"] = (t_first, time.time())
+    return out
+
+
 # --------------------------------------------------------------- reference
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -297,7 +368,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline (0 = skip)")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "backward"],
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "backward", "decode_variants"],
                     help="run one part of the step only (small profiling runs)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward-pass leg (timed after the step, reported under 'backward')")
@@ -334,6 +405,7 @@ def main():
         wp = dataclasses.replace(wp, H=args.prefill_h, name=f"{wp.name}_h{args.prefill_h}")
     # the backward pass takes no key mask: it is timed on the unpadded workloads
     do_b = args.only in ("all", "backward") and not args.no_backward and not wp.pad_heads
+    do_v = args.only in ("all", "decode_variants")
     modes = list(wp.causal_modes)
     wd = W.WORKLOADS[DECODE]
     if args.decode_b:
@@ -406,10 +478,13 @@ def main():
     if fa.device_status() != fa.FA_OK:
         raise RuntimeError("device status not OK after the timed region")
     bwd = run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, world, rank, dev) if do_b else None
+    dvar = run_decode_variants(args, fa, W, stream, warm, world, rank, dev) if do_v else None
     sampler.stop()
     clocks = sampler.summary((t_wall0, t_wall1))
     if bwd is not None:
         bwd["clocks"] = sampler.summary(bwd.pop("_window"))
+    if dvar is not None:
+        dvar["clocks"] = sampler.summary(dvar.pop("_window"))
 
     nm = len(modes)
     t_modes = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / 1e3 for i in range(nm)]
@@ -539,6 +614,11 @@ def main():
         line["backward"] = bwd
         if not do_p and not do_d:
             line["value"] = bwd["value"]
+    if dvar is not None:
+        line["decode_variants"] = dvar
+        if not do_p and not do_d and bwd is None:
+            first = next(iter(dvar["workloads"].values()))
+            line["value"], line["unit"] = first["value"], "GB/s"
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
