@@ -269,6 +269,9 @@ def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
     out = {"workloads": {}}
     t_first = None
     for key, w in W.DECODE_VARIANTS.items():
+        if args.dv_b:
+            import dataclasses
+            w = dataclasses.replace(w, B=args.dv_b, name=w.name.replace("b64", f"b{args.dv_b}"))
         q, k, v, lens = W.make_decode_inputs(w, seed=3000 + rank, device="cuda")
         ws = torch.empty(fa.decode_grouped_workspace_size(w.B, w.H, w.Nq, w.d, w.num_splits), dtype=torch.uint8,
                          device=dev)
@@ -374,6 +377,7 @@ def main():
                     help="skip the backward-pass leg (timed after the step, reported under 'backward')")
     ap.add_argument("--decode-b", type=int, default=0, help="override the decode batch (profiling a small case)")
     ap.add_argument("--prefill-h", type=int, default=0, help="override the prefill heads (profiling a small case)")
+    ap.add_argument("--dv-b", type=int, default=0, help="override the decode-variant batch (profiling a small case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--prefill-workload", default=PREFILL,
                     choices=["prefill_2k", "prefill_8k", "prefill_32k", "prefill_32k_pad"],
