@@ -259,6 +259,60 @@ def run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, worl
     return out
 
 
+def run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, dev):
+    """Time the materialising baseline (cuBLAS S = scale Q K^T in bf16, this
+    library's row softmax writing P over S, cuBLAS O = P V) on the prefill
+    workload's inputs, per causal mode, L2 flushed between steps."""
+    import torch
+    import torch.distributed as dist
+    ws = torch.empty(fa.materialized_workspace_size(wp.B, wp.H, wp.Nq, wp.Nk), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(wp.B, wp.H, wp.Nq, dtype=torch.float32, device=dev)
+
+    def call(c):
+        fa.fwd_materialized(q, k, v, scale=wp.scale, causal=c, workspace=ws, out=o, lse=lse)
+
+    for _ in range(warm):
+        flush.zero_()
+        for c in modes:
+            call(c)
+    torch.cuda.synchronize()
+    K, nm = args.steps, len(modes)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nm + 1)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, c in enumerate(modes):
+            call(c)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    tm = torch.tensor([sum(e[j].elapsed_time(e[j + 1]) for e in ev) / 1e3 for j in range(nm)],
+                      dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+    tm = tm.tolist()
+    fm = [wp.flops(c) for c in modes]
+    # the pages' count: scores written, read, probabilities written, read (2-byte), plus Q, K, V, O
+    nbytes = 4 * wp.B * wp.H * wp.Nq * wp.Nk * 2 + wp.io_bytes()
+    out = {"value": world * K * sum(fm) / sum(tm) / 1e12, "unit": "TFLOP/s", "ms": sum(tm) / K * 1e3,
+           "hbm_bytes_model_per_launch": nbytes, "fused_min_bytes_per_launch": wp.io_bytes(),
+           "gbs_model": K * nm * nbytes / sum(tm) / 1e9,
+           "what": "cuBLAS bf16 GEMM S = scale Q K^T -> row softmax (this library, P over S) -> cuBLAS O = P V",
+           "_window": (t0, t1), "_t_modes": tm}
+    for c, t, f in zip(modes, tm, fm):
+        tag = "causal" if c else "noncausal"
+        out[f"ms_{tag}"] = t / K * 1e3
+        out[f"tflops_{tag}"] = K * f / t / 1e12
+    return out
+
+
 def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
     """Time fa_decode_grouped on each decode-variant workload (grouped K/V
     heads, ragged lengths, 1 or 4 new tokens). Inputs are drawn on the device
@@ -371,7 +425,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline (0 = skip)")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "backward", "decode_variants"],
+    ap.add_argument("--only", default="all",
+                    choices=["all", "prefill", "decode", "backward", "decode_variants", "materialized"],
                     help="run one part of the step only (small profiling runs)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward-pass leg (timed after the step, reported under 'backward')")
@@ -410,12 +465,13 @@ def main():
     # the backward pass takes no key mask: it is timed on the unpadded workloads
     do_b = args.only in ("all", "backward") and not args.no_backward and not wp.pad_heads
     do_v = args.only in ("all", "decode_variants")
+    do_m = args.only in ("all", "materialized") and not wp.pad_heads
     modes = list(wp.causal_modes)
     wd = W.WORKLOADS[DECODE]
     if args.decode_b:
         import dataclasses
         wd = dataclasses.replace(wd, B=args.decode_b, name=wd.name.replace("b64", f"b{args.decode_b}"))
-    if do_p or do_b:
+    if do_p or do_b or do_m:
         q, k, v = W.make_qkv(wp.B, wp.H, wp.Nq, wp.Nk, wp.d, seed=rank, device="cuda")
         o = torch.empty_like(q)
         lse = torch.empty(wp.B, wp.H, wp.Nq, dtype=torch.float32, device=dev)
@@ -483,12 +539,15 @@ def main():
         raise RuntimeError("device status not OK after the timed region")
     bwd = run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, world, rank, dev) if do_b else None
     dvar = run_decode_variants(args, fa, W, stream, warm, world, rank, dev) if do_v else None
+    mat = run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, dev) if do_m else None
     sampler.stop()
     clocks = sampler.summary((t_wall0, t_wall1))
     if bwd is not None:
         bwd["clocks"] = sampler.summary(bwd.pop("_window"))
     if dvar is not None:
         dvar["clocks"] = sampler.summary(dvar.pop("_window"))
+    if mat is not None:
+        mat["clocks"] = sampler.summary(mat.pop("_window"))
 
     nm = len(modes)
     t_modes = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / 1e3 for i in range(nm)]
@@ -618,6 +677,12 @@ def main():
         line["backward"] = bwd
         if not do_p and not do_d:
             line["value"] = bwd["value"]
+    if mat is not None:
+        t_mat = mat.pop("_t_modes")
+        if do_p:  # how many times faster the fused kernel ran, per mode
+            mat["fused_speedup"] = {("causal" if c else "noncausal"): tmm / tm
+                                    for c, tm, tmm in zip(modes, t_modes, t_mat)}
+        line["materialized"] = mat
     if dvar is not None:
         line["decode_variants"] = dvar
         if not do_p and not do_d and bwd is None:

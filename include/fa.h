@@ -165,6 +165,32 @@ fa_status fa_decode_grouped(const void* q, const void* k_cache, const void* v_ca
                             float* lse, int B, int H, int Hkv, int Nq, int Nk, int d, float scale, int num_splits,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace fa_fwd_materialized needs: the bf16 score /
+ * probability matrix [B, H, Nq, Nk], rounded up to 256 bytes. 0 for invalid
+ * arguments. */
+size_t fa_materialized_workspace_size(int B, int H, int Nq, int Nk);
+
+/* The materialising baseline the IO argument compares against ("Explain
+ * FlashAttention ...", section "What the byte arithmetic does and does not
+ * say"): S = scale * Q K^T is written to HBM in bf16, read back by a row
+ * softmax that writes P (bf16, over S), and P is read again for O = P V.
+ * Four N^2-sized transfers of 2-byte values, against the fused fa_fwd's
+ * none. It computes the same attention as fa_fwd (without a key mask), with
+ * S and P rounded to bf16. The two products are cuBLAS GEMMs (the library
+ * opens libcublas.so.13 on first use and keeps one cuBLAS handle per device;
+ * calls are serialised inside the library); the softmax is this library's
+ * kernel.
+ *   q, o      bf16 [B, H, Nq, d]       k, v  bf16 [B, H, Nk, d]
+ *   lse       fp32 [B, H, Nq] (natural log; may be NULL)
+ *   workspace device memory of at least fa_materialized_workspace_size()
+ *             bytes, 256-byte aligned, owned by the caller; overwritten.
+ * Errors: as for fa_fwd, plus FA_ERR_UNSUPPORTED when Nk is not a multiple of
+ * 8 or exceeds the row held in one CTA's shared memory (about 116k keys), or
+ * when cuBLAS cannot be loaded; FA_ERR_WORKSPACE. */
+fa_status fa_fwd_materialized(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                              int Nk, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
 /* Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator of
  * B*H*ceil(Nq/128)*128*d elements (Nq padded to whole 128-row tiles) and two
  * fp32 per-row statistics [B, H, Nq], each rounded up to 256 bytes. Returns 0

@@ -22,7 +22,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfa_gb300.so")
-SOURCES = ["fa_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "backward_sm103.cu", "decode_grouped_sm103.cu"]
+SOURCES = ["fa_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "backward_sm103.cu", "decode_grouped_sm103.cu",
+           "materialized_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -73,7 +74,8 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
                 raise RuntimeError(f"nvcc failed on {src}")
             objs.append(obj)
     tmp = LIB + ".tmp"
-    cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
+    # cuBLAS (the materialising baseline's GEMMs) is opened at run time with dlopen, not linked
+    cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static", "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if verbose or r.returncode != 0:
         sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)

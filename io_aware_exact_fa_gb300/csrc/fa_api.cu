@@ -14,7 +14,11 @@
 #include <mutex>
 
 #include "fa.h"
+#include <cublas_v2.h>
+#include <dlfcn.h>
+
 #include "decode_grouped.cuh"
+#include "materialized.cuh"
 #include "fa_common.cuh"
 
 #ifndef FA_TAIL_SPLIT
@@ -82,6 +86,8 @@ fa_status device_state(DeviceState** out) {
     if ((e = fa::prefill_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
     if ((e = fa::bwd_set_attributes(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=64)");
     if ((e = fa::bwd_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=128)");
+    if ((e = fa::materialized_set_attributes()) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(materialized softmax)");
     if ((e = fa::decode_grouped_set_attributes(64)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(grouped decode d=64)");
     if ((e = fa::decode_grouped_set_attributes(128)) != cudaSuccess)
@@ -349,6 +355,121 @@ fa_status fa_decode_grouped(const void* q, const void* k_cache, const void* v_ca
   m.S = num_splits;
   if ((e = fa::launch_decode_merge(d, m, s)) != cudaSuccess) return cuda_fail(e, "grouped decode merge launch");
   t_launches += 2;
+  return FA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Materialising baseline: two cuBLAS GEMMs around the row-softmax kernel.
+// cuBLAS is opened on first use (the library itself does not link it), with
+// one handle per device; calls are serialised on a mutex because the handle's
+// stream is set per call.
+namespace {
+
+struct CublasApi {
+  bool tried = false;
+  bool ok = false;
+  decltype(&cublasCreate_v2) create = nullptr;
+  decltype(&cublasSetStream_v2) set_stream = nullptr;
+  // the exported C symbol (32-bit sizes); the C++ header also declares a 64-bit overload
+  using gemm_t = cublasStatus_t (*)(cublasHandle_t, cublasOperation_t, cublasOperation_t, int, int, int, const void*,
+                                    const void*, cudaDataType, int, long long int, const void*, cudaDataType, int,
+                                    long long int, const void*, void*, cudaDataType, int, long long int, int,
+                                    cublasComputeType_t, cublasGemmAlgo_t);
+  gemm_t gemm = nullptr;
+  cublasHandle_t handle[kMaxDevices] = {};
+};
+CublasApi g_cublas;
+std::mutex g_cublas_mu;
+
+// Returns the device's handle, or nullptr with the error detail set.
+cublasHandle_t cublas_handle(int dev) {
+  if (!g_cublas.tried) {
+    g_cublas.tried = true;
+    void* lib = nullptr;
+    for (const char* name : {"libcublas.so.13", "libcublas.so"})
+      if ((lib = dlopen(name, RTLD_NOW | RTLD_LOCAL)) != nullptr) break;
+    if (lib) {
+      g_cublas.create = reinterpret_cast<decltype(g_cublas.create)>(dlsym(lib, "cublasCreate_v2"));
+      g_cublas.set_stream = reinterpret_cast<decltype(g_cublas.set_stream)>(dlsym(lib, "cublasSetStream_v2"));
+      g_cublas.gemm = reinterpret_cast<CublasApi::gemm_t>(dlsym(lib, "cublasGemmStridedBatchedEx"));
+      g_cublas.ok = g_cublas.create && g_cublas.set_stream && g_cublas.gemm;
+    }
+  }
+  if (!g_cublas.ok) {
+    fail(FA_ERR_UNSUPPORTED, "cuBLAS (libcublas.so.13) could not be loaded");
+    return nullptr;
+  }
+  if (!g_cublas.handle[dev]) {
+    cublasHandle_t h = nullptr;
+    if (g_cublas.create(&h) != CUBLAS_STATUS_SUCCESS) {
+      fail(FA_ERR_CUDA, "cublasCreate failed");
+      return nullptr;
+    }
+    g_cublas.handle[dev] = h;
+  }
+  return g_cublas.handle[dev];
+}
+
+}  // namespace
+
+size_t fa_materialized_workspace_size(int B, int H, int Nq, int Nk) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 0;
+  return (static_cast<size_t>(B) * H * Nq * Nk * 2 + 255) & ~size_t(255);
+}
+
+fa_status fa_fwd_materialized(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                              int Nk, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  t_detail[0] = 0;
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1)
+    return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Nq >= 1, Nk >= 1 (got %d %d %d %d)", B, H, Nq, Nk);
+  if (fa_status s = check_scale(scale)) return s;
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
+  if (Nk % 8 != 0 || Nk > fa::MATERIALIZED_MAX_NK)
+    return fail(FA_ERR_UNSUPPORTED, "the materialising baseline takes Nk a multiple of 8 and at most %d (got %d)",
+                fa::MATERIALIZED_MAX_NK, Nk);
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > INT_MAX || BH * Nq > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B * H * Nq is too large");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return fail(FA_ERR_UNSUPPORTED, "q, k, v, o must be 16-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(FA_ERR_UNSUPPORTED, "lse must be 4-byte aligned");
+  const size_t need = fa_materialized_workspace_size(B, H, Nq, Nk);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+    return fail(FA_ERR_WORKSPACE, "workspace must be 256-byte aligned and >= %zu bytes", need);
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_cublas_mu);
+  cublasHandle_t h = cublas_handle(dev);
+  if (!h) return g_cublas.ok ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g_cublas.set_stream(h, s) != CUBLAS_STATUS_SUCCESS) return fail(FA_ERR_CUDA, "cublasSetStream failed");
+  // Row-major S [Nq, Nk] is column-major S^T = K Q^T: A = K (row-major [Nk, d], read transposed), B = Q.
+  const float alpha = scale, beta = 0.f, one = 1.f;
+  cublasStatus_t cs = g_cublas.gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, Nk, Nq, d, &alpha, k, CUDA_R_16BF, d,
+                                    static_cast<long long>(Nk) * d, q, CUDA_R_16BF, d,
+                                    static_cast<long long>(Nq) * d, &beta, workspace, CUDA_R_16BF, Nk,
+                                    static_cast<long long>(Nq) * Nk, static_cast<int>(BH), CUBLAS_COMPUTE_32F,
+                                    CUBLAS_GEMM_DEFAULT);
+  if (cs != CUBLAS_STATUS_SUCCESS) return fail(FA_ERR_CUDA, "cublasGemmStridedBatchedEx (scores) failed: %d", cs);
+  fa::MaterializedParams mp{};
+  mp.s = workspace;
+  mp.lse = lse;
+  mp.rows = BH * Nq;
+  mp.Nq = Nq;
+  mp.Nk = Nk;
+  mp.causal = causal ? 1 : 0;
+  if ((e = fa::launch_materialized_softmax(mp, s)) != cudaSuccess) return cuda_fail(e, "materialized softmax");
+  // Row-major O [Nq, d] is column-major O^T = V^T P^T: A = V (column-major [d, Nk]), B = P (column-major [Nk, Nq]).
+  cs = g_cublas.gemm(h, CUBLAS_OP_N, CUBLAS_OP_N, d, Nq, Nk, &one, v, CUDA_R_16BF, d,
+                     static_cast<long long>(Nk) * d, workspace, CUDA_R_16BF, Nk, static_cast<long long>(Nq) * Nk,
+                     &beta, o, CUDA_R_16BF, d, static_cast<long long>(Nq) * d, static_cast<int>(BH),
+                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  if (cs != CUBLAS_STATUS_SUCCESS) return fail(FA_ERR_CUDA, "cublasGemmStridedBatchedEx (values) failed: %d", cs);
+  t_launches += 1;  // the softmax kernel; the two GEMMs are cuBLAS's
   return FA_OK;
 }
 

@@ -42,6 +42,8 @@ EXPORTS = {
     "fa_decode_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_decode_grouped_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_decode_grouped": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
+    "fa_materialized_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fa_fwd_materialized": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_get_device_status": (_i, [_vp]),
@@ -224,6 +226,37 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                                         lse.data_ptr() if lse is not None else None, B, H, Nk, d, float(scale),
                                         int(num_splits), _stream_ptr(stream))
     _check(rc, "fa_decode_splitkv_noalloc")
+    return out, lse
+
+
+def materialized_workspace_size(B: int, H: int, Nq: int, Nk: int) -> int:
+    return int(_lib.fa_materialized_workspace_size(B, H, Nq, Nk))
+
+
+def fwd_materialized(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+                     causal: bool = False, workspace: Optional[torch.Tensor] = None,
+                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The materialising baseline (fa.h fa_fwd_materialized): S and P through HBM in bf16."""
+    _need(q, "q"); _need(k, "k"); _need(v, "v")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = materialized_workspace_size(B, H, Nq, Nk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, Nq, dtype=torch.float32, device=q.device)
+    _need(out, "out"); _need(lse, "lse", torch.float32)
+    rc = _lib.fa_fwd_materialized(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq,
+                                  Nk, d, float(scale), int(bool(causal)), workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(rc, "fa_fwd_materialized")
     return out, lse
 
 
