@@ -53,17 +53,26 @@ struct BwdCfg {
   static constexpr int BOX_BYTES = 128 * 128;     // one TMA box: 128 rows x 64 bf16
   static constexpr int NBOX = D / 64;
   static constexpr int DS_BYTES = 128 * 128 * 2;  // dS^T tile: 128 keys x 128 queries bf16
+  // At d = 64, P^T and dQ_i get TMEM columns of their own and dS^T two shared
+  // buffers, so the next step's S^T and dP^T need not wait for this step's
+  // products; at d = 128 neither fits.
+  static constexpr bool SEP = (D == 64);
+  static constexpr int NDS = SEP ? 2 : 1;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;                 // 2 stages of (Q, dO)
-  static constexpr int DS_OFF = Q_OFF + 2 * 2 * TILE_BYTES;
-  static constexpr int STAT_OFF = DS_OFF + DS_BYTES;               // lse2[128], Dv[128]
+  static constexpr int DS_OFF = Q_OFF + 2 * 2 * TILE_BYTES;        // NDS dS^T buffers
+  static constexpr int STAT_OFF = DS_OFF + NDS * DS_BYTES;         // lse2[128], Dv[128]
   static constexpr int BAR_OFF = STAT_OFF + 2 * 128 * 4;
   static constexpr int NBAR = 16;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t ST_COL = 0, DPT_COL = 128, DV_COL = 256, DK_COL = 256 + D;
+  // P^T (bf16, 64 columns): inside S^T at d = 128 (half h at 64 h), its own columns at d = 64 (half h at 32 h);
+  // dQ_i: in the dP^T columns at d = 128, its own columns at d = 64
+  static constexpr uint32_t PT_COL = SEP ? 384 : ST_COL, PT_HALF = SEP ? 32 : 64;
+  static constexpr uint32_t DQ_COL = SEP ? 448 : DPT_COL;
   static constexpr uint32_t IDESC_T = idesc_bf16_f32(128, 128, false);        // K-major A and B
   static constexpr uint32_t IDESC_B_MN = idesc_bf16_f32(128, D, true);        // B MN-major
   static constexpr uint32_t IDESC_AB_MN = idesc_bf16_f32(128, D, true, true); // A and B MN-major
@@ -159,18 +168,18 @@ __global__ void __launch_bounds__(256) fa_bwd_finish_kernel(const float* __restr
 // ----------------------------------------------------- softmax-grad half tile
 // One thread, one key row, one half (64 query columns, chunks 2h and 2h + 1) of
 // a 128 x 128 step: P^T = exp2(S^T * scale * log2(e) - lse2) and
-// dS^T = P^T * (dP^T - D). P^T (bf16) goes over S^T columns [64h, 64h + 32),
+// dS^T = P^T * (dP^T - D). P^T (bf16) goes to the P^T columns of half h,
 // dS^T (bf16) into the 128-byte-swizzled shared tile (box h). nlse2 and ndrow
 // hold -lse2 and -D per query column. With MASK, columns below c_lo are
 // masked. One exponential pair in four runs on the FMA pipe (exp2_fma2) to
 // offload the MUFU unit. before_math() is called once, after the first TMEM
-// loads are issued and before the statistics are read; before_store() once,
-// before the first shared-memory store. If either returns false the step
-// stops there.
-template <int D, bool MASK, typename F, typename G>
-__device__ __forceinline__ bool sg_half(uint32_t tST, uint32_t tDPT, uint32_t ds_row, int row, int h, int c_lo,
-                                        const float* nlse2, const float* ndrow, float sl2, G&& before_math,
-                                        F&& before_store) {
+// loads are issued and before the statistics are read; before_pstore() once,
+// before the first P^T store; before_store() once, before the first
+// shared-memory store. If any returns false the step stops there.
+template <int D, bool MASK, typename F, typename G, typename E>
+__device__ __forceinline__ bool sg_half(uint32_t tST, uint32_t tDPT, uint32_t tPT, uint32_t ds_row, int row, int h,
+                                        int c_lo, const float* nlse2, const float* ndrow, float sl2, G&& before_math,
+                                        E&& before_pstore, F&& before_store) {
   using C = BwdCfg<D>;
   const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
@@ -222,9 +231,10 @@ __device__ __forceinline__ bool sg_half(uint32_t tST, uint32_t tDPT, uint32_t ds
       dk[2 * j] = pack_bf16x2(d0, d1);
       dk[2 * j + 1] = pack_bf16x2(d2, d3);
     }
-    // P^T over S^T columns this thread already read: half h keeps its 64
-    // queries (32 bf16x2 columns) at column 64 h, inside its own S^T columns
-    tmem_st16(tST + h * 64 + cc * 16, pk);
+    // P^T: half h keeps its 64 queries (32 bf16x2 columns) at tPT + PT_HALF h;
+    // at d = 128 that is inside the S^T columns this thread already read
+    if (cc == 0 && !before_pstore()) return false;
+    tmem_st16(tPT + h * C::PT_HALF + cc * 16, pk);
     if (cc == 0 && !before_store()) return false;
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
@@ -347,8 +357,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     __syncwarp();
   } else if (warp == BWD_MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    // Per step i: dQ_i, dV_i, then (for step i + 1) S^T and dP^T, then dK_i,
-    // so the next step's softmax-grad starts while dK_i runs.
+    // Per step i at d = 128: dQ_i, dV_i, then (for step i + 1) S^T and dP^T,
+    // then dK_i, so the next step's softmax-grad starts while dK_i runs. At
+    // d = 64 (separate P^T and dQ columns, two dS^T buffers): the next step's
+    // S^T and dP^T first, then dV_i, dQ_i and dK_i, so the next softmax-grad
+    // overlaps all three.
     const bool leader = lane == 0;
     bool ok = true;
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
@@ -360,9 +373,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     constexpr uint32_t DHI = sdesc_sw128_hi(1024);
     const uint32_t k_lo = sdesc_sw128_lo(smem_u32(sK), 16), kmn_lo = sdesc_sw128_lo(smem_u32(sK), C::BOX_BYTES);
     const uint32_t v_lo = sdesc_sw128_lo(smem_u32(sV), 16);
-    const uint32_t ds_lo = sdesc_sw128_lo(smem_u32(sDS), 16), dsmn_lo = sdesc_sw128_lo(smem_u32(sDS), C::BOX_BYTES);
     const uint32_t tST = tmem + C::ST_COL, tDPT = tmem + C::DPT_COL, tDV = tmem + C::DV_COL,
-                   tDK = tmem + C::DK_COL;
+                   tDK = tmem + C::DK_COL, tPT = tmem + C::PT_COL, tDQ = tmem + C::DQ_COL;
+    auto ds_base = [&](int it) { return smem_u32(sDS) + (C::NDS > 1 ? (it & 1) * C::DS_BYTES : 0); };
     // K-major K-step kk of a tile: (kk / 4) boxes plus (kk % 4) x 32 bytes in;
     // MN-major K-step kk: 16 rows = 2048 bytes in (64-column boxes LBO apart)
     auto kmaj = [](int kk) { return static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4); };
@@ -377,8 +390,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_w(tST, k_lo + kmaj(kk), DHI, q_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
       }
-      // dP^T (the dP^T columns) only after the previous dQ_i was read out
-      if (it > 0 && !wait_bar(dq_free, (it - 1) & 1)) return false;
+      // at d = 128, dP^T (the dP^T columns) only after the previous dQ_i was read out
+      if (!C::SEP && it > 0 && !wait_bar(dq_free, (it - 1) & 1)) return false;
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -393,33 +406,57 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     for (int it = 0; ok && it < n_it; ++it) {
       const uint32_t qb = stage(it);
       const uint32_t qmn_lo = sdesc_sw128_lo(qb, C::BOX_BYTES), domn_lo = sdesc_sw128_lo(qb + C::TILE_BYTES, C::BOX_BYTES);
-      if (!wait_bar(p_full, it & 1)) break;
-      if (leader) {
-        // dQ_i = dS K (A = dS, the MN-major view of dS^T; B = K MN-major), into the dP^T columns
+      const uint32_t ds_lo = sdesc_sw128_lo(ds_base(it), 16), dsmn_lo = sdesc_sw128_lo(ds_base(it), C::BOX_BYTES);
+      // dQ_i = dS K (A = dS, the MN-major view of dS^T; B = K MN-major)
+      auto issue_dq = [&]() {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss_w(tDPT, dsmn_lo + mnmaj(kk), DHI, kmn_lo + mnmaj(kk), DHI, C::IDESC_AB_MN, kk > 0 ? 1u : 0u);
+          mma_ss_w(tDQ, dsmn_lo + mnmaj(kk), DHI, kmn_lo + mnmaj(kk), DHI, C::IDESC_AB_MN, kk > 0 ? 1u : 0u);
         mma_commit(dq_full);
-        // dV += P^T dO_i (A = P^T from TMEM: queries 16kk.. at column 8kk
-        // for the first half, 64 + 8(kk - 4) for the second; B = dO_i MN-major)
+      };
+      // dV += P^T dO_i (A = P^T from TMEM: queries 16 kk.. of half kk / 4 at
+      // tPT + PT_HALF (kk / 4) + 8 (kk % 4); B = dO_i MN-major)
+      auto issue_dv = [&]() {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts_w(tDV, tST + kk * 8 + (kk >= 4 ? 32 : 0), domn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tDV, tPT + (kk >> 2) * C::PT_HALF + (kk & 3) * 8, domn_lo + mnmaj(kk), DHI, C::IDESC_B_MN,
+                   (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(dv_done);
-      }
-      if (it + 1 < n_it) {
-        // the next S^T overwrites P^T_i: only after dV_i read it
-        if (!wait_bar(q_full + ((it + 1) & 1), ((it + 1) >> 1) & 1)) break;
-        if (!wait_bar(dv_done, it & 1)) break;
-        if (!issue_s_dp(it + 1)) break;
-      }
-      if (leader) {
-        // dK += dS^T Q_i (A = dS^T K-major, B = Q_i MN-major)
+      };
+      // dK += dS^T Q_i (A = dS^T K-major, B = Q_i MN-major)
+      auto issue_dk = [&]() {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss_w(tDK, ds_lo + kmaj(kk), DHI, qmn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(step_done);
         mma_commit(q_empty + (it & 1));
+      };
+      if (!wait_bar(p_full, it & 1)) break;
+      if constexpr (C::SEP) {
+        // the softmax-grad has read S^T_i and dP^T_i: the next step's products may overwrite them
+        if (it + 1 < n_it) {
+          if (!wait_bar(q_full + ((it + 1) & 1), ((it + 1) >> 1) & 1)) break;
+          if (!issue_s_dp(it + 1)) break;
+        }
+        if (leader) issue_dv();
+        // dQ_i into the dQ columns once the drain has read dQ_{i-1}
+        if (it > 0 && !wait_bar(dq_free, (it - 1) & 1)) break;
+        if (leader) {
+          issue_dq();
+          issue_dk();
+        }
+      } else {
+        if (leader) {
+          issue_dq();  // into the dP^T columns, so its drain overlaps dV and dK
+          issue_dv();
+        }
+        if (it + 1 < n_it) {
+          // the next S^T overwrites P^T_i: only after dV_i read it
+          if (!wait_bar(q_full + ((it + 1) & 1), ((it + 1) >> 1) & 1)) break;
+          if (!wait_bar(dv_done, it & 1)) break;
+          if (!issue_s_dp(it + 1)) break;
+        }
+        if (leader) issue_dk();
       }
     }
     if (leader) {
@@ -439,7 +476,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tST = tmem + lane_base + C::ST_COL, tDPT = tmem + lane_base + C::DPT_COL;
     bool ok = true;
-    const uint32_t ds_row = smem_u32(sDS) + static_cast<uint32_t>(row) * 128u;
+    const uint32_t tPT = tmem + lane_base + C::PT_COL;
+    // this thread's key row in dS^T buffer b
+    auto ds_row = [&](int it) {
+      return smem_u32(sDS) + (C::NDS > 1 ? (it & 1) * C::DS_BYTES : 0) + static_cast<uint32_t>(row) * 128u;
+    };
     // one entry of the per-row statistics (h = 0: lse2, h = 1: D) of query
     // row `row` of the Q tile, loaded one step ahead
     const float* stat_src = h ? p.drow : p.lse2;
@@ -469,10 +510,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       };
       // dS^T in shared memory is rewritten only after the previous step's dK
       // (its last reader) completed
+      // At d = 128 dS^T is rewritten only after the previous step's dK (its
+      // last reader) completed. At d = 64 this step's buffer was last read by
+      // step i-2's dQ and dK, which completed before S^T_i (their commit order
+      // covers them), so no wait.
       auto before_store = [&]() {
-        if (it == 0) return true;
+        if (C::SEP || it == 0) return true;
         bool w = mbar_wait(step_done, (it - 1) & 1, lim, p.status, abort_flag);
         return __all_sync(0xffffffffu, w) != 0;
+      };
+      // At d = 64 P^T has columns of its own, which dV_{i-1} reads: wait for it.
+      // At d = 128 P^T goes over S^T_i, which was written after dV_{i-1} completed.
+      auto before_pstore = [&]() {
+        if (!C::SEP || it == 0) return true;
+        bool w = mbar_wait(dv_done, (it - 1) & 1, lim, p.status, abort_flag);
+        w = __all_sync(0xffffffffu, w) != 0;
+        tc_fence_after();
+        return w;
       };
       // Only a Q tile that crosses the causal diagonal (query q sees this key
       // iff q >= kabs - delta) or a key tile past Nk needs a per-element test.
@@ -481,11 +535,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // lse = +inf, so their weights are 0 without a test.
       if ((p.causal && k0 + 127 - delta > q0) || k0 + 128 > p.Nk) {
         const int c_lo = kabs >= p.Nk ? INT_MAX : (p.causal ? kabs - delta - q0 : INT_MIN);
-        ok = sg_half<D, true>(tST, tDPT, ds_row, row, h, c_lo, s_nlse2, s_ndrow, p.scale_log2, before_math,
-                              before_store);
+        ok = sg_half<D, true>(tST, tDPT, tPT, ds_row(it), row, h, c_lo, s_nlse2, s_ndrow, p.scale_log2, before_math,
+                              before_pstore, before_store);
       } else {
-        ok = sg_half<D, false>(tST, tDPT, ds_row, row, h, 0, s_nlse2, s_ndrow, p.scale_log2, before_math,
-                               before_store);
+        ok = sg_half<D, false>(tST, tDPT, tPT, ds_row(it), row, h, 0, s_nlse2, s_ndrow, p.scale_log2, before_math,
+                               before_pstore, before_store);
       }
       if (!ok) break;
       tmem_st_wait();
@@ -530,7 +584,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // -------------------------------------------------------------- dQ drain
     const int wq = warp & 3;
     const int row = wq * 32 + lane;  // query row within the Q tile
-    const uint32_t src = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::DPT_COL;
+    const uint32_t src = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::DQ_COL;
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
       ok = mbar_wait(dq_full, it & 1, lim, p.status, abort_flag);
