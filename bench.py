@@ -259,6 +259,60 @@ def run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, worl
     return out
 
 
+def e2e_prefill(fa, wp, modes, q, k, v, keep_words, mstrides, n_e, dev):
+    """End-to-end prefill through the public API: every step copies q, k, v
+    from pinned host memory, runs the forward pass per causal mode and copies
+    o and lse back. Two device buffer sets and three streams (upload, compute,
+    read-back) pipeline consecutive steps; events order each set's reuse.
+    Returns the seconds from the first upload to the last read-back."""
+    import torch
+    hin = [x.cpu().pin_memory() for x in (q, k, v)]
+    nm = len(modes)
+    hout = [(torch.empty(tuple(q.shape), dtype=q.dtype).pin_memory(),
+             torch.empty((wp.B, wp.H, wp.Nq), dtype=torch.float32).pin_memory()) for _ in modes]
+    din = [[torch.empty_like(x) for x in (q, k, v)] for _ in range(2)]
+    dout = [[(torch.empty_like(q), torch.empty((wp.B, wp.H, wp.Nq), dtype=torch.float32, device=dev))
+             for _ in modes] for _ in range(2)]
+    # one upload stream per input tensor, so the copies can run on several copy engines at once
+    s_ins = [torch.cuda.Stream() for _ in hin]
+    s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [[torch.cuda.Event() for _ in hin] for _ in range(n_e)]
+    comp_done = [torch.cuda.Event() for _ in range(n_e)]
+    out_done = [torch.cuda.Event() for _ in range(n_e)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    t0.record(cur)
+    for st in (*s_ins, s_comp, s_out):
+        st.wait_event(t0)
+    for i in range(n_e):
+        b = i % 2
+        for st, dst, src, ev in zip(s_ins, din[b], hin, in_done[i]):
+            with torch.cuda.stream(st):
+                if i >= 2:
+                    st.wait_event(comp_done[i - 2])  # set b's inputs were last read by step i-2
+                dst.copy_(src, non_blocking=True)
+                ev.record(st)
+        for ev in in_done[i]:
+            s_comp.wait_event(ev)
+        if i >= 2:
+            s_comp.wait_event(out_done[i - 2])  # set b's outputs were last read back by step i-2
+        for c, causal in enumerate(modes):
+            fa.fwd(*din[b], scale=wp.scale, causal=causal, keep_bits=keep_words, mask_strides=mstrides,
+                   out=dout[b][c][0], lse=dout[b][c][1], stream=s_comp)
+        comp_done[i].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[i])
+            for c in range(nm):
+                hout[c][0].copy_(dout[b][c][0], non_blocking=True)
+                hout[c][1].copy_(dout[b][c][1], non_blocking=True)
+            out_done[i].record(s_out)
+    cur.wait_event(out_done[n_e - 1])
+    t1.record(cur)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / 1e3
+
+
 def run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, dev):
     """Time the materialising baseline (cuBLAS S = scale Q K^T in bf16, this
     library's row softmax writing P over S, cuBLAS O = P V) on the prefill
@@ -568,9 +622,7 @@ def main():
         n_e = max(3, min(K, 20))
         ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_e)]
         if do_p:
-            hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
-            ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in modes]
-            hl = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in modes]
+            te_p = e2e_prefill(fa, wp, modes, q, k, v, keep_words, mstrides, n_e, dev)
         if do_d:
             hdq = dq.cpu().pin_memory()
             hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
@@ -579,14 +631,6 @@ def main():
         for i in range(n_e):
             flush.zero_()
             ee[i][0].record(stream)
-            if do_p:
-                q.copy_(hq, non_blocking=True)
-                k.copy_(hk, non_blocking=True)
-                v.copy_(hv, non_blocking=True)
-                for c, causal in enumerate(modes):
-                    prefill(causal)
-                    ho[c].copy_(o, non_blocking=True)
-                    hl[c].copy_(lse, non_blocking=True)
             ee[i][1].record(stream)
             if do_d:
                 dq.copy_(hdq, non_blocking=True)
@@ -595,12 +639,15 @@ def main():
                 hdl.copy_(dlse, non_blocking=True)
             ee[i][2].record(stream)
         torch.cuda.synchronize()
-        te_p = sum(e[0].elapsed_time(e[1]) for e in ee) / 1e3
         te_d = sum(e[1].elapsed_time(e[2]) for e in ee) / 1e3
         if do_p:
             e2e = {"value": world * n_e * f_p / te_p / 1e12, "unit": "TFLOP/s",
                    "h2d_bytes_per_step": 3 * q.numel() * 2,
-                   "d2h_bytes_per_step": nm * (o.numel() * 2 + lse.numel() * 4)}
+                   "d2h_bytes_per_step": nm * (o.numel() * 2 + lse.numel() * 4),
+                   "steps": n_e,
+                   "note": "each step uploads q, k, v from pinned host memory and reads o, lse back; two device "
+                           "buffer sets on upload (one stream per tensor), compute and read-back streams let step i+1's upload "
+                           "and step i-1's read-back overlap step i's kernels; no L2 flush (uploads land in L2)"}
         if do_d:
             dec_e2e = {"value": world * n_e * dec_bytes / te_d / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": dq.numel() * 2, "d2h_bytes_per_step": do.numel() * 2 + dlse.numel() * 4,
