@@ -65,7 +65,7 @@ struct DgCfg {
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = TILE;  // stage s: K at KV_OFF + 2 s TILE, V right after
   static constexpr int BAR_OFF = KV_OFF + NS * 2 * TILE;
-  static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1;
+  static constexpr int NBAR = 1 + 2 * NS + 2 + 2 + 1 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -92,6 +92,10 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
   uint64_t* s_full = bars + 1 + 2 * C::NS;  // [2] S_j computed
   uint64_t* p_full = s_full + 2;            // [2] P_j stored (all 128 softmax threads)
   uint64_t* o_done = p_full + 2;            // PV_j completed (one phase per key tile)
+  // The last PV completed. The epilogue gets a barrier of its own: the softmax
+  // may finish the last tile while o_done is still short of the last two PVs,
+  // and a parity wait cannot tell a phase two ahead.
+  uint64_t* o_last = o_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -117,6 +121,7 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
       mbar_init(p_full + i, 128);
     }
     mbar_init(o_done, 1);
+    mbar_init(o_last, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -211,6 +216,7 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
           mma_ts_w(tmem + C::O_COL, tP + kk * 8, v_lo + mnmaj(kk), DHI, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(o_done);
         mma_commit(kv_empty + j % C::NS);
+        if (j == n - 1) mma_commit(o_last);
       }
     }
     if (leader && n > 0) mbar_drain(o_done, (n - 1) & 1, lim);  // every MMA completed before TMEM is released
@@ -304,7 +310,7 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
     }
     // ---- epilogue: the unnormalised partial (o, m, l) of this split
     if (ok && n > 0) {
-      ok = mbar_wait(o_done, (n - 1) & 1, lim, p.status, abort_flag);
+      ok = mbar_wait(o_last, 0, lim, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
     }
