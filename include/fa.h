@@ -185,7 +185,7 @@ size_t fa_materialized_workspace_size(int B, int H, int Nq, int Nk);
  *   workspace device memory of at least fa_materialized_workspace_size()
  *             bytes, 256-byte aligned, owned by the caller; overwritten.
  * Errors: as for fa_fwd, plus FA_ERR_UNSUPPORTED when Nk is not a multiple of
- * 8 or exceeds the row held in one CTA's shared memory (about 116k keys), or
+ * 8 or exceeds the row held in one CTA's shared memory (about 58k keys), or
  * when cuBLAS cannot be loaded; FA_ERR_WORKSPACE. */
 fa_status fa_fwd_materialized(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                               int Nk, int d, float scale, int causal, void* workspace, size_t workspace_bytes,

@@ -17,7 +17,7 @@ struct MaterializedParams {
 
 cudaError_t launch_materialized_softmax(const MaterializedParams& p, cudaStream_t stream);
 cudaError_t materialized_set_attributes();
-// largest Nk one CTA's shared memory holds (one bf16 row)
-constexpr int MATERIALIZED_MAX_NK = (227 * 1024) / 2 - 64;
+// largest Nk one CTA's shared memory holds (one fp32 row)
+constexpr int MATERIALIZED_MAX_NK = (227 * 1024) / 4 - 64;
 
 }  // namespace fa
