@@ -67,7 +67,7 @@ def visible_pair_fraction(wp, causal: bool) -> float:
 
 
 # headers a kernel source includes besides fa_ptx.cuh and fa_common.cuh
-KERNEL_HEADERS = {"decode_grouped_sm103.cu": ("decode_grouped.cuh",)}
+KERNEL_HEADERS = {"decode_grouped_sm103.cu": ("decode_grouped.cuh",), "materialized_sm103.cu": ("materialized.cuh",)}
 
 
 def kernel_hash(name: str) -> str:
@@ -359,6 +359,7 @@ def run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, d
            "hbm_bytes_model_per_launch": nbytes, "fused_min_bytes_per_launch": wp.io_bytes(),
            "gbs_model": K * nm * nbytes / sum(tm) / 1e9,
            "what": "cuBLAS bf16 GEMM S = scale Q K^T -> row softmax (this library, P over S) -> cuBLAS O = P V",
+           "softmax_traffic": recorded_traffic("materialized_sm103.cu", wp.name + "_materialized_softmax"),
            "_window": (t0, t1), "_t_modes": tm}
     for c, t, f in zip(modes, tm, fm):
         tag = "causal" if c else "noncausal"
