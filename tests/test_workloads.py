@@ -76,3 +76,31 @@ def test_sample_rows():
     r = W.sample_rows(1000, 50, seed=1)
     assert r.shape == (50,) and len(set(r.tolist())) == 50 and torch.all(r[1:] > r[:-1])
     assert torch.equal(r, W.sample_rows(1000, 50, seed=1))
+
+
+def test_backward_flop_convention():
+    w = W.WORKLOADS["prefill_8k"]
+    # five products of 2*Nq*Nk*d per (b, h): 2.5x the forward's two
+    assert w.bwd_flops(False) == 10 * 1 * 32 * 8192 * 8192 * 128
+    assert w.bwd_flops(True) == w.bwd_flops(False) / 2
+
+
+def test_decode_variant_inputs():
+    import dataclasses
+    w = dataclasses.replace(W.DECODE_VARIANTS["gqa_spec"], B=3, Nk=512, len_lo=200)
+    q, k, v, lens = W.make_decode_inputs(w, seed=5)
+    assert q.shape == (3, 32, 4, 128) and k.shape == (3, 8, 512, 128) and v.shape == k.shape
+    assert q.dtype == torch.bfloat16 and lens.dtype == torch.int32 and lens.shape == (3,)
+    assert int(lens.min()) >= 200 and int(lens.max()) <= 512
+    again = W.make_decode_inputs(w, seed=5)
+    assert all(torch.equal(a, b) for a, b in zip((q, k, v, lens), again))
+    # q, k, v come first from the generator, exactly as make_qkv draws them for a square case
+    g = torch.Generator().manual_seed(5)
+    assert torch.equal(q, torch.randn(3, 32, 4, 128, generator=g).to(torch.bfloat16))
+
+
+def test_decode_variant_bytes():
+    w = W.DECODE_VARIANTS["gqa"]
+    lens = [4096, 8192, 0, 9000]  # clamped to [0, Nk]
+    kv = 2 * w.Hkv * w.d * 2 * (4096 + 8192 + 0 + 8192)
+    assert w.io_bytes(lens) == kv + 2 * w.B * w.H * w.Nq * w.d * 2 + 4 * w.B * w.H * w.Nq
