@@ -66,6 +66,33 @@ def visible_pair_fraction(wp, causal: bool) -> float:
     return (wp.pad_heads * padded + (wp.H - wp.pad_heads) * full) / (wp.H * full)
 
 
+def max_over_ranks(times, world: int, device):
+    """Element-wise maximum of per-rank device times (seconds) over all ranks:
+    the job lasts as long as its slowest rank. With world == 1 the times come
+    back unchanged; otherwise every rank receives the maxima (an all-reduce on
+    `device`, a CUDA device under NCCL, the CPU under gloo)."""
+    import torch
+    t = torch.tensor([float(x) for x in times], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_step: float, steps: int, seconds: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas that each process
+    `units_per_step` per step for `steps` steps, the slowest taking `seconds`
+    (weak scaling: every rank does the same per-rank work)."""
+    return world * steps * units_per_step / seconds
+
+
+def barrier(world: int):
+    """Line all ranks up at the edges of a timed region (no-op for one rank)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
 # headers a kernel source includes besides fa_ptx.cuh and fa_common.cuh
 KERNEL_HEADERS = {"decode_grouped_sm103.cu": ("decode_grouped.cuh",), "materialized_sm103.cu": ("materialized.cuh",)}
 
@@ -195,7 +222,6 @@ def run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, worl
     inputs, once per causal mode per step, with its own events and L2 flush;
     dO is seeded N(0,1) bf16 and O, lse come from the forward pass."""
     import torch
-    import torch.distributed as dist
     gen = torch.Generator().manual_seed(2000 + rank)
     dout = torch.randn(tuple(q.shape), generator=gen).to(torch.bfloat16).to(dev)
     fo = {}
@@ -218,8 +244,7 @@ def run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, worl
     K, nm = args.steps, len(modes)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nm + 1)] for _ in range(K)]
     n0 = fa.launch_count()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
     for i in range(K):
@@ -229,21 +254,17 @@ def run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, worl
             backward(c)
             ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     t1 = time.time()
     launches = fa.launch_count() - n0
     if fa.device_status() != fa.FA_OK:
         raise RuntimeError("device status not OK after the backward timed region")
-    tm = torch.tensor([sum(e[j].elapsed_time(e[j + 1]) for e in ev) / 1e3 for j in range(nm)],
-                      dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-    tm = tm.tolist()
+    tm = max_over_ranks([sum(e[j].elapsed_time(e[j + 1]) for e in ev) / 1e3 for j in range(nm)], world, dev)
     fm = [wp.bwd_flops(c) for c in modes]
     ach = K * sum(fm) / sum(tm) / 1e12
     peaks = measured_peaks()
-    out = {"value": world * ach, "unit": "TFLOP/s", "ms": sum(tm) / K * 1e3, "gpu_launches": launches,
+    out = {"value": whole_job_rate(sum(fm), K, sum(tm), world) / 1e12, "unit": "TFLOP/s", "ms": sum(tm) / K * 1e3,
+           "gpu_launches": launches,
            "dout": "N(0,1) bf16, seeded; O and lse from fa_fwd",
            "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": ach / peaks["bf16_tflops"],
@@ -318,7 +339,6 @@ def run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, d
     library's row softmax writing P over S, cuBLAS O = P V) on the prefill
     workload's inputs, per causal mode, L2 flushed between steps."""
     import torch
-    import torch.distributed as dist
     ws = torch.empty(fa.materialized_workspace_size(wp.B, wp.H, wp.Nq, wp.Nk), dtype=torch.uint8, device=dev)
     o = torch.empty_like(q)
     lse = torch.empty(wp.B, wp.H, wp.Nq, dtype=torch.float32, device=dev)
@@ -333,8 +353,7 @@ def run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, d
     torch.cuda.synchronize()
     K, nm = args.steps, len(modes)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nm + 1)] for _ in range(K)]
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
     for i in range(K):
@@ -344,18 +363,13 @@ def run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, d
             call(c)
             ev[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     t1 = time.time()
-    tm = torch.tensor([sum(e[j].elapsed_time(e[j + 1]) for e in ev) / 1e3 for j in range(nm)],
-                      dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-    tm = tm.tolist()
+    tm = max_over_ranks([sum(e[j].elapsed_time(e[j + 1]) for e in ev) / 1e3 for j in range(nm)], world, dev)
     fm = [wp.flops(c) for c in modes]
     # the pages' count: scores written, read, probabilities written, read (2-byte), plus Q, K, V, O
     nbytes = 4 * wp.B * wp.H * wp.Nq * wp.Nk * 2 + wp.io_bytes()
-    out = {"value": world * K * sum(fm) / sum(tm) / 1e12, "unit": "TFLOP/s", "ms": sum(tm) / K * 1e3,
+    out = {"value": whole_job_rate(sum(fm), K, sum(tm), world) / 1e12, "unit": "TFLOP/s", "ms": sum(tm) / K * 1e3,
            "hbm_bytes_model_per_launch": nbytes, "fused_min_bytes_per_launch": wp.io_bytes(),
            "gbs_model": K * nm * nbytes / sum(tm) / 1e9,
            "what": "cuBLAS bf16 GEMM S = scale Q K^T -> row softmax (this library, P over S) -> cuBLAS O = P V",
@@ -373,7 +387,6 @@ def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
     heads, ragged lengths, 1 or 4 new tokens). Inputs are drawn on the device
     with the workload recipe; the K/V caches (2 GB) exceed L2, so no flush."""
     import torch
-    import torch.distributed as dist
     peaks = measured_peaks()
     out = {"workloads": {}}
     t_first = None
@@ -398,8 +411,7 @@ def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
             raise RuntimeError("device status not OK after the decode-variant warm-up")
         K = args.steps
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
-        if world > 1:
-            dist.barrier()
+        barrier(world)
         torch.cuda.synchronize()
         t0 = time.time()
         t_first = t_first or t0
@@ -409,19 +421,15 @@ def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
             call()
             ev[i + 1].record(stream)
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        barrier(world)
         launches = fa.launch_count() - n0
         if fa.device_status() != fa.FA_OK:
             raise RuntimeError("device status not OK after the decode-variant timed region")
-        tt = torch.tensor([ev[0].elapsed_time(ev[K]) / 1e3], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = tt.item()
+        t = max_over_ranks([ev[0].elapsed_time(ev[K]) / 1e3], world, dev)[0]
         nbytes = w.io_bytes(lens.tolist())
         ach = K * nbytes / t / 1e9
         out["workloads"][w.name] = {
-            "value": world * ach, "unit": "GB/s", "ms": t / K * 1e3, "bytes": nbytes, "gpu_launches": launches,
+            "value": whole_job_rate(nbytes, K, t, world) / 1e9, "unit": "GB/s", "ms": t / K * 1e3, "bytes": nbytes, "gpu_launches": launches,
             "config": {"B": w.B, "H": w.H, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
                        "num_splits": w.num_splits, "seqlens": f"uniform in [{w.len_lo}, {w.Nk}], seeded",
                        "mean_seqlen": float(lens.float().mean().item())},
@@ -578,16 +586,14 @@ def main():
     sampler.start()
     time.sleep(0.2)
     launches0 = fa.launch_count()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
     for i in range(K):
         flush.zero_()                     # outside the events: evicts the prefill inputs from L2
         step_body(ev[i])
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+    barrier(world)
     t_wall1 = time.time()
     launches = fa.launch_count() - launches0
     if fa.device_status() != fa.FA_OK:
@@ -607,10 +613,7 @@ def main():
     nm = len(modes)
     t_modes = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / 1e3 for i in range(nm)]
     t_d = sum(e[nm].elapsed_time(e[nm + 1]) for e in ev) / 1e3
-    times = torch.tensor(t_modes + [t_d], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    times = times.tolist()
+    times = max_over_ranks(t_modes + [t_d], world, dev)
     t_modes, t_d = times[:nm], times[nm]
     f_modes = [wp.flops(c) for c in modes]
     t_p, f_p = sum(t_modes), sum(f_modes)
@@ -641,8 +644,9 @@ def main():
             ee[i][2].record(stream)
         torch.cuda.synchronize()
         te_d = sum(e[1].elapsed_time(e[2]) for e in ee) / 1e3
+        te_p, te_d = max_over_ranks([te_p if do_p else 0.0, te_d], world, dev)
         if do_p:
-            e2e = {"value": world * n_e * f_p / te_p / 1e12, "unit": "TFLOP/s",
+            e2e = {"value": whole_job_rate(f_p, n_e, te_p, world) / 1e12, "unit": "TFLOP/s",
                    "h2d_bytes_per_step": 3 * q.numel() * 2,
                    "d2h_bytes_per_step": nm * (o.numel() * 2 + lse.numel() * 4),
                    "steps": n_e,
@@ -650,7 +654,7 @@ def main():
                            "buffer sets on upload (one stream per tensor), compute and read-back streams let step i+1's upload "
                            "and step i-1's read-back overlap step i's kernels; no L2 flush (uploads land in L2)"}
         if do_d:
-            dec_e2e = {"value": world * n_e * dec_bytes / te_d / 1e9, "unit": "GB/s",
+            dec_e2e = {"value": whole_job_rate(dec_bytes, n_e, te_d, world) / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": dq.numel() * 2, "d2h_bytes_per_step": do.numel() * 2 + dlse.numel() * 4,
                        "note": "KV cache resident on the device; q in, o and lse out per step"}
 
@@ -668,7 +672,7 @@ def main():
         return 0
     line = {
         "metric": METRIC,
-        "value": world * K * f_p / t_p / 1e12 if do_p else None,
+        "value": whole_job_rate(f_p, K, t_p, world) / 1e12 if do_p else None,
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": K,
@@ -712,7 +716,7 @@ def main():
             line["roofline"]["tflops_effective"] = ach * share
     if do_d:
         ach = K * dec_bytes / t_d / 1e9
-        line["decode"] = {"value": world * ach, "unit": "GB/s", "ms": t_d / K * 1e3, "bytes": dec_bytes,
+        line["decode"] = {"value": whole_job_rate(dec_bytes, K, t_d, world) / 1e9, "unit": "GB/s", "ms": t_d / K * 1e3, "bytes": dec_bytes,
                           "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                        "frac": ach / peaks["hbm_gbs"],
                                        "traffic": recorded_traffic("decode_sm103.cu", wd.name),
