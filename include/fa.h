@@ -86,6 +86,39 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
                         const uint32_t* keep_bits, int64_t mstride_b, int64_t mstride_h,
                         int64_t mstride_q, void* stream);
 
+/* Bytes of device workspace fa_fwd_host needs: two buffer sets, each holding
+ * q, k, v, o and lse of one chunk of heads (every region rounded up to 256
+ * bytes). chunk_heads <= 0 selects the default, ceil(B*H / 4) heads. Returns 0
+ * for invalid arguments. */
+size_t fa_fwd_host_workspace_size(int B, int H, int Nq, int Nk, int d, int chunk_heads);
+
+/* fa_fwd on HOST buffers: q, k, v, o and lse have the layouts above but live
+ * in host memory. The B*H heads (contiguous in that layout) are processed in
+ * chunks of chunk_heads. Each chunk's q, k and v are copied into one of two
+ * device buffer sets in the workspace, and its forward pass runs there. Its o
+ * and lse are then copied back. Upload, compute and read-back of consecutive
+ * chunks overlap: they run on library-owned streams (three upload streams,
+ * one compute stream per buffer set, one read-back stream), one set of
+ * streams per host thread and device. The call is ordered after the work
+ * already queued on `stream`, and `stream` waits for the last read-back. The
+ * outputs are complete once `stream` has been synchronised; the inputs must
+ * stay unchanged until then.
+ *
+ * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to overlap the kernels. Pageable memory gives the same results
+ * with serialised copies.
+ *
+ * workspace: device memory, 256-byte aligned, at least
+ * fa_fwd_host_workspace_size(...) bytes, not used by anything else until
+ * `stream` reaches the end of the call. Errors: those of fa_fwd (host
+ * pointers need no alignment), and FA_ERR_WORKSPACE for a NULL, short or
+ * misaligned workspace. A CUDA failure after some chunks were queued returns
+ * FA_ERR_CUDA; `stream` still waits for the queued work, and the outputs are
+ * undefined. */
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                      int chunk_heads, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace fa_decode_splitkv needs: fp32 partial
  * (o[d], m, l) per (b, h, split), i.e. B*H*num_splits*(d + 2)*4 rounded up
  * to 256. Returns 0 for invalid arguments. */

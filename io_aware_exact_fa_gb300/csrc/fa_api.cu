@@ -136,6 +136,66 @@ fa_status check_scale(float scale) {
   return FA_OK;
 }
 
+// Streams and events of the host-buffer forward pass, one set per host
+// thread and device (so concurrent callers on different threads never share
+// them). Created on first use and kept for the life of the process.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t up[3] = {nullptr, nullptr, nullptr};  // q, k, v uploads (several copy engines)
+  cudaStream_t comp[2] = {nullptr, nullptr};         // one per device buffer set
+  cudaStream_t down = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t up_done[2][3] = {};
+  cudaEvent_t comp_done[2] = {};
+  cudaEvent_t down_done[2] = {};
+};
+thread_local HostPipe t_pipe[kMaxDevices];
+
+fa_status host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = t_pipe[dev];
+  if (!hp.ready) {
+    cudaError_t e = cudaSuccess;
+    for (auto& s : hp.up)
+      if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e, "stream");
+    for (auto& s : hp.comp)
+      if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e, "stream");
+    if ((e = cudaStreamCreateWithFlags(&hp.down, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e, "stream");
+    cudaEvent_t* evs[] = {&hp.start,         &hp.up_done[0][0], &hp.up_done[0][1], &hp.up_done[0][2],
+                          &hp.up_done[1][0], &hp.up_done[1][1], &hp.up_done[1][2], &hp.comp_done[0],
+                          &hp.comp_done[1],  &hp.down_done[0],  &hp.down_done[1]};
+    for (cudaEvent_t* ev : evs)
+      if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e, "event");
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FA_OK;
+}
+
+// Byte layout of one device buffer set of the host-buffer forward pass:
+// q, k, v, o, lse of `ch` heads, each region 256-byte aligned.
+struct HostSet {
+  size_t q, k, v, o, lse, bytes;
+};
+HostSet host_set_layout(long long ch, int Nq, int Nk, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  HostSet h{};
+  const size_t qb = up(static_cast<size_t>(ch) * Nq * d * 2), kb = up(static_cast<size_t>(ch) * Nk * d * 2);
+  h.q = 0;
+  h.k = h.q + qb;
+  h.v = h.k + kb;
+  h.o = h.v + kb;
+  h.lse = h.o + qb;
+  h.bytes = h.lse + up(static_cast<size_t>(ch) * Nq * 4);
+  return h;
+}
+// Heads per chunk: the caller's choice, else a quarter of B*H. Fewer, larger
+// chunks keep every chunk's launch wide enough to fill the GPU; four still
+// let the uploads of one chunk overlap the kernel of the previous one.
+long long host_chunk_heads(long long BH, int chunk_heads) {
+  const long long ch = chunk_heads > 0 ? chunk_heads : (BH + 3) / 4;
+  return std::max(1LL, std::min(ch, BH));
+}
+
 }  // namespace
 
 // Set the calling thread's error detail (used by entry points in other files).
@@ -236,6 +296,102 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
                  int d, float scale, int causal, void* stream) {
   return fa_fwd_masked(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, nullptr, 0, 0, 0, stream);
+}
+
+size_t fa_fwd_host_workspace_size(int B, int H, int Nq, int Nk, int d, int chunk_heads) {
+  if (B < 1 || H < 1 || Nq < 0 || Nk < 1 || (d != 64 && d != 128)) return 0;
+  const long long ch = host_chunk_heads(static_cast<long long>(B) * H, chunk_heads);
+  return 2 * host_set_layout(ch, Nq, Nk, d).bytes;
+}
+
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                      int Nk, int d, float scale, int causal, int chunk_heads, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  t_detail[0] = 0;
+  if (B < 1 || H < 1 || Nk < 1 || Nq < 0)
+    return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Nk >= 1, Nq >= 0 (got %d %d %d %d)", B, H, Nk, Nq);
+  if (fa_status s = check_scale(scale)) return s;
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
+  if (Nq == 0) return FA_OK;
+  if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > INT_MAX) return fail(FA_ERR_INVALID_ARG, "B*H is too large");
+  const long long ch = host_chunk_heads(BH, chunk_heads);
+  const HostSet L = host_set_layout(ch, Nq, Nk, d);
+  if (workspace == nullptr || workspace_bytes < 2 * L.bytes)
+    return fail(FA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace_bytes, 2 * L.bytes);
+  if (!aligned(workspace, 256)) return fail(FA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  HostPipe* hp = nullptr;
+  if (fa_status s = host_pipe(dev, &hp)) return s;
+
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // everything below is ordered after the work already queued on `stream`
+  if ((e = cudaEventRecord(hp->start, cs)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  for (cudaStream_t s2 : {hp->up[0], hp->up[1], hp->up[2], hp->comp[0], hp->comp[1], hp->down})
+    if ((e = cudaStreamWaitEvent(s2, hp->start, 0)) != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+
+  // On a failure after work was queued, `stream` still waits for whatever
+  // the internal streams had been given, so later work on it stays ordered.
+  auto join = [&](fa_status s2) {
+    for (cudaStream_t x : {hp->up[0], hp->up[1], hp->up[2], hp->comp[0], hp->comp[1], hp->down})
+      if (cudaEventRecord(hp->start, x) == cudaSuccess) cudaStreamWaitEvent(cs, hp->start, 0);
+    return s2;
+  };
+  const size_t qrow = static_cast<size_t>(Nq) * d * 2, krow = static_cast<size_t>(Nk) * d * 2;
+  const uint8_t* hin[3] = {static_cast<const uint8_t*>(q), static_cast<const uint8_t*>(k),
+                           static_cast<const uint8_t*>(v)};
+  const size_t per_head[3] = {qrow, krow, krow};
+  const long long nchunks = (BH + ch - 1) / ch;
+  for (long long c = 0; c < nchunks; ++c) {
+    const int sidx = static_cast<int>(c & 1);
+    uint8_t* set = static_cast<uint8_t*>(workspace) + sidx * L.bytes;
+    const long long h0 = c * ch, nh = std::min(ch, BH - h0);
+    uint8_t* din[3] = {set + L.q, set + L.k, set + L.v};
+    // uploads into set sidx, once chunk c-2's kernel has finished reading it
+    for (int t = 0; t < 3; ++t) {
+      if (c >= 2 && (e = cudaStreamWaitEvent(hp->up[t], hp->comp_done[sidx], 0)) != cudaSuccess)
+        return join(cuda_fail(e, "cudaStreamWaitEvent"));
+      if ((e = cudaMemcpyAsync(din[t], hin[t] + h0 * per_head[t], nh * per_head[t], cudaMemcpyHostToDevice,
+                               hp->up[t])) != cudaSuccess)
+        return join(cuda_fail(e, "cudaMemcpyAsync(host to device)"));
+      if ((e = cudaEventRecord(hp->up_done[sidx][t], hp->up[t])) != cudaSuccess)
+        return join(cuda_fail(e, "cudaEventRecord"));
+    }
+    // the chunk's forward pass, once its inputs landed and chunk c-2's
+    // outputs have been read back from this set
+    cudaStream_t comp = hp->comp[sidx];
+    for (int t = 0; t < 3; ++t)
+      if ((e = cudaStreamWaitEvent(comp, hp->up_done[sidx][t], 0)) != cudaSuccess)
+        return join(cuda_fail(e, "cudaStreamWaitEvent"));
+    if (c >= 2 && (e = cudaStreamWaitEvent(comp, hp->down_done[sidx], 0)) != cudaSuccess)
+      return join(cuda_fail(e, "cudaStreamWaitEvent"));
+    float* dlse = lse ? reinterpret_cast<float*>(set + L.lse) : nullptr;
+    if (fa_status s2 = fa_fwd(din[0], din[1], din[2], set + L.o, dlse, 1, static_cast<int>(nh), Nq, Nk, d, scale,
+                              causal, comp))
+      return join(s2);
+    if ((e = cudaEventRecord(hp->comp_done[sidx], comp)) != cudaSuccess)
+      return join(cuda_fail(e, "cudaEventRecord"));
+    // read-back of the chunk's o and lse
+    if ((e = cudaStreamWaitEvent(hp->down, hp->comp_done[sidx], 0)) != cudaSuccess)
+      return join(cuda_fail(e, "cudaStreamWaitEvent"));
+    if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(o) + h0 * qrow, set + L.o, nh * qrow, cudaMemcpyDeviceToHost,
+                             hp->down)) != cudaSuccess)
+      return join(cuda_fail(e, "cudaMemcpyAsync(device to host)"));
+    if (lse && (e = cudaMemcpyAsync(lse + h0 * Nq, dlse, nh * Nq * sizeof(float), cudaMemcpyDeviceToHost,
+                                    hp->down)) != cudaSuccess)
+      return join(cuda_fail(e, "cudaMemcpyAsync(device to host)"));
+    if ((e = cudaEventRecord(hp->down_done[sidx], hp->down)) != cudaSuccess)
+      return join(cuda_fail(e, "cudaEventRecord"));
+  }
+  // the read-back stream runs the chunks in order: its last event covers them all
+  if ((e = cudaStreamWaitEvent(cs, hp->down_done[(nchunks - 1) & 1], 0)) != cudaSuccess)
+    return join(cuda_fail(e, "cudaStreamWaitEvent"));
+  return FA_OK;
 }
 
 size_t fa_decode_workspace_size(int B, int H, int d, int num_splits) {

@@ -37,6 +37,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_E
 EXPORTS = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i64, _i64, _i64, _vp]),
+    "fa_fwd_host_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "fa_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
     "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fa_decode_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _sz, _vp]),
     "fa_decode_splitkv_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
@@ -124,6 +126,59 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float
                                 B, H, Nq, Nk, d, float(scale), int(bool(causal)),
                                 keep_bits.data_ptr(), int(sb), int(sh), int(sq), st)
         _check(rc, "fa_fwd_masked")
+    return out, lse
+
+
+def fwd_host_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int, chunk_heads: int = 0) -> int:
+    return int(_lib.fa_fwd_host_workspace_size(B, H, Nq, Nk, d, chunk_heads))
+
+
+def _need_host(t: torch.Tensor, name: str, dtype=torch.bfloat16) -> None:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+             causal: bool = False, chunk_heads: int = 0, workspace: Optional[torch.Tensor] = None,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, with_lse: bool = True,
+             stream: Optional[torch.cuda.Stream] = None,
+             sync: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """fa_fwd_host: the forward pass on HOST tensors (q [B,H,Nq,d], k/v [B,H,Nk,d]
+    bf16; pin them for overlap). The library copies chunks of heads to the
+    current CUDA device, runs the fused kernel there and copies o and lse
+    back. With ``sync`` the call waits for ``stream`` before returning;
+    otherwise the host outputs are complete once the stream is synchronised."""
+    _need_host(q, "q"); _need_host(k, "k"); _need_host(v, "v")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != (B, H, Nk, d):
+        raise ValueError("k and v must be [B, H, Nk, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(tuple(q.shape), dtype=q.dtype, pin_memory=pin)
+    _need_host(out, "out")
+    if with_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=pin)
+    if lse is not None:
+        _need_host(lse, "lse", torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(1, fwd_host_workspace_size(B, H, Nq, Nk, d, chunk_heads)), dtype=torch.uint8,
+                                device="cuda")
+    _need(workspace, "workspace", torch.uint8)
+    st = _stream_ptr(stream)
+    rc = _lib.fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, float(scale),
+                          int(bool(causal)), int(chunk_heads), workspace.data_ptr(),
+                          workspace.numel(), st)
+    _check(rc, "fa_fwd_host")
+    if sync:
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return out, lse
 
 

@@ -113,6 +113,34 @@ def test_decode_validation(lib):
     assert g(P, P, P, P, None, 1, 1, 8, 64, 0.1, 4, P + 16, big, None) == 5     # workspace misaligned
 
 
+def test_fwd_host_workspace_and_validation(lib):
+    """The host-buffer forward pass: workspace size (two sets of q, k, v, o, lse
+    per chunk of heads, each region rounded to 256 bytes) and the checks made
+    before any CUDA call."""
+    ws = lib.fa_fwd_host_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [ctypes.c_int] * 6
+    up = lambda x: (x + 255) // 256 * 256
+    # B=4 H=16 -> 64 heads, default chunk = 16 heads
+    q, kv, lse = up(16 * 2048 * 64 * 2), up(16 * 2048 * 64 * 2), up(16 * 2048 * 4)
+    assert ws(4, 16, 2048, 2048, 64, 0) == 2 * (2 * q + 2 * kv + lse)
+    assert ws(4, 16, 2048, 2048, 64, 1000) == ws(4, 16, 2048, 2048, 64, 64)  # clamped to B*H
+    assert ws(1, 3, 100, 300, 128, 2) == 2 * (2 * up(2 * 100 * 256) + 2 * up(2 * 300 * 256) + up(2 * 100 * 4))
+    assert ws(1, 1, 8, 8, 96, 0) == 0 and ws(0, 1, 8, 8, 64, 0) == 0 and ws(1, 1, 8, 0, 64, 0) == 0
+    f = lib.fa_fwd_host
+    f.restype = ctypes.c_int
+    f.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
+    P, big = 1 << 20, 1 << 30
+    assert f(None, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, 0, P, big, None) == 1       # NULL q
+    assert f(P, P, P, P, None, 1, 1, 8, 8, 64, -1.0, 0, 0, P, big, None) == 1           # scale < 0
+    assert f(P, P, P, P, None, 1, 1, 8, 8, 80, 0.125, 0, 0, P, big, None) == 2          # d = 80
+    assert f(P, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, 0, None, big, None) == 5       # no workspace
+    assert f(P, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, 0, P, 64, None) == 5           # too small
+    assert f(P, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, 0, P + 16, big, None) == 5     # misaligned
+    assert f(None, None, None, None, None, 1, 1, 0, 8, 64, 0.125, 0, 0, None, 0, None) == 0  # Nq = 0
+
+
 def test_wait_limit_roundtrip(lib):
     lib.fa_get_wait_limit_ns.restype = ctypes.c_uint64
     lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
