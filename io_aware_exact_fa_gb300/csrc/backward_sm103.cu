@@ -58,6 +58,10 @@ struct BwdCfg {
   // products; at d = 128 neither fits.
   static constexpr bool SEP = (D == 64);
   static constexpr int NDS = SEP ? 2 : 1;
+  // At d = 64 (where it measured faster) only lane 0 of the MMA warp walks
+  // the issue loop: its waits need no warp vote, and lanes 1-31 wait once, at
+  // the end, for the drain.
+  static constexpr bool SOLO_ISSUE = (D == 64);
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;                 // 2 stages of (Q, dO)
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     bool ok = true;
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
       ok = mbar_wait(bar, parity, lim, p.status, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
+      if (!C::SOLO_ISSUE) ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
       return ok;
     };
@@ -400,10 +404,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       return true;
     };
-    if (n_it > 0) {
+    const bool walks = !C::SOLO_ISSUE || leader;  // this lane runs the issue loop
+    if (n_it > 0 && walks) {
       if (wait_bar(kv_full, 0) && wait_bar(q_full, 0)) issue_s_dp(0);
     }
-    for (int it = 0; ok && it < n_it; ++it) {
+    for (int it = 0; ok && walks && it < n_it; ++it) {
       const uint32_t qb = stage(it);
       const uint32_t qmn_lo = sdesc_sw128_lo(qb, C::BOX_BYTES), domn_lo = sdesc_sw128_lo(qb + C::TILE_BYTES, C::BOX_BYTES);
       const uint32_t ds_lo = sdesc_sw128_lo(ds_base(it), 16), dsmn_lo = sdesc_sw128_lo(ds_base(it), C::BOX_BYTES);

@@ -79,6 +79,12 @@ namespace fa {
 #ifndef FA_O_STAGE
 #define FA_O_STAGE 1             // separate O staging buffers where shared memory allows (d = 64)
 #endif
+#ifndef FA_SOLO_ISSUE_D64
+#define FA_SOLO_ISSUE_D64 1      // lane 0 of each issuer warp runs the MMA loop alone (no warp votes)
+#endif
+#ifndef FA_SOLO_ISSUE_D128
+#define FA_SOLO_ISSUE_D128 0
+#endif
 #ifndef FA_STAGGER_MIN_TILES
 #define FA_STAGGER_MIN_TILES 8   // only units this long amortise the delayed start
 #endif
@@ -132,6 +138,10 @@ struct PrefillCfg {
   // and one CTA per unit is faster.
   static constexpr bool PERSIST = (D == 64) ? FA_PERSIST_D64 : FA_PERSIST_D128;
   static constexpr bool UNIT_DONE_EARLY = (D == 64) ? FA_UNIT_DONE_EARLY_D64 : FA_UNIT_DONE_EARLY_D128;
+  // Where it measured faster (d = 64), only lane 0 of each MMA-issuing warp
+  // walks the issue loop: its waits then need no warp vote, and lanes 1-31
+  // wait once, at the end, for the drain.
+  static constexpr bool SOLO_ISSUE = (D == 64) ? FA_SOLO_ISSUE_D64 : FA_SOLO_ISSUE_D128;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -434,8 +444,9 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       // One warp per Q tile (tile 0 first). tcgen05.mma issue only runs about
       // one instruction ahead of the tensor pipe, so every barrier wait or
       // commit of a lone issuing warp would leave the pipe idle; with two
-      // issuers each one's waits overlap the other's MMAs. The whole warp runs
-      // the loop and waits; lane 0 issues MMAs and commits.
+      // issuers each one's waits overlap the other's MMAs. Lane 0 issues the
+      // MMAs and commits; with SOLO_ISSUE it also runs the loop alone,
+      // otherwise the whole warp runs it and votes on every wait.
       const int t = warp - PREFILL_MMA_WARP0;
       const uint32_t sQa = smem_u32(sQ) + t * C::TILE_BYTES;
       // Low descriptor words of Q_t, K slot 0 and V slot 0 (every operand
@@ -455,7 +466,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 
       auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
         ok = mbar_wait(bar, parity, lim, p.status, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
+        if (!C::SOLO_ISSUE) ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         return ok;
       };
@@ -471,14 +482,14 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           pb = pa;
         }
         ok = (a == nullptr) || mbar_wait2(a, pa, b, pb, lim, p.status, abort_flag, c, pc);
-        ok = __all_sync(0xffffffffu, ok);
+        if (!C::SOLO_ISSUE) ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         return ok;
       };
 
       int g0 = 0;          // key tiles of earlier units (ring position)
       int c0 = 0, c1 = 0;  // steps of tile 0 / tile 1 in earlier units
-      for (int k = 0; ok; ++k) {
+      for (int k = 0; ok && (!C::SOLO_ISSUE || lane == 0); ++k) {
         const int u = unit_at(k);
         if (u >= U) break;
         const Unit w = unit_info(p, u, kv_keep);
