@@ -582,8 +582,10 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 
         // Ping-pong: the following Q tile starts once the leader's first
         // softmax is done, so one tile's exponentials overlap the other tile's
-        // MMAs instead of both tiles competing for the same unit at once.
-        if (C::STAGGER && t != lead && n_lead >= FA_STAGGER_MIN_TILES && nt > 0 &&
+        // MMAs instead of both tiles competing for the same unit at once. Not
+        // under a causal mask, where the two tiles' key ranges differ and the
+        // delayed start measured slower.
+        if (C::STAGGER && !p.causal && t != lead && n_lead >= FA_STAGGER_MIN_TILES && nt > 0 &&
             !wait_bar(p_full + lead, c_lead & 1))
           break;
 
