@@ -280,7 +280,7 @@ def run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, worl
     return out
 
 
-def e2e_prefill(fa, wp, modes, q, k, v, n_e, dev):
+def e2e_prefill(fa, wp, modes, q, k, v, n_e, dev, chunk_heads=0):
     """End-to-end prefill through the host-buffer entry point fa_fwd_host.
     Each step makes one call per causal mode on pinned host q, k, v; every
     call uploads the inputs in chunks of heads, runs the fused kernel on each
@@ -295,15 +295,15 @@ def e2e_prefill(fa, wp, modes, q, k, v, n_e, dev):
     hin = [x.cpu().pin_memory() for x in (q, k, v)]
     hout = [(torch.empty(tuple(q.shape), dtype=q.dtype).pin_memory(),
              torch.empty((wp.B, wp.H, wp.Nq), dtype=torch.float32).pin_memory()) for _ in modes]
-    wsb = fa.fwd_host_workspace_size(wp.B, wp.H, wp.Nq, wp.Nk, wp.d)
+    wsb = fa.fwd_host_workspace_size(wp.B, wp.H, wp.Nq, wp.Nk, wp.d, chunk_heads)
     ws = [torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in modes]
     req = [torch.cuda.Stream() for _ in modes]
     cur = torch.cuda.current_stream()
 
     def step():
         for c, causal in enumerate(modes):
-            fa.fwd_host(*hin, scale=wp.scale, causal=causal, workspace=ws[c], out=hout[c][0], lse=hout[c][1],
-                        stream=req[c], sync=False)
+            fa.fwd_host(*hin, scale=wp.scale, causal=causal, chunk_heads=chunk_heads, workspace=ws[c],
+                        out=hout[c][0], lse=hout[c][1], stream=req[c], sync=False)
 
     step()  # warm-up: creates the library's copy streams
     torch.cuda.synchronize()
@@ -483,6 +483,8 @@ def main():
     ap.add_argument("--prefill-h", type=int, default=0, help="override the prefill heads (profiling a small case)")
     ap.add_argument("--dv-b", type=int, default=0, help="override the decode-variant batch (profiling a small case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--e2e-chunk-heads", type=int, default=0,
+                    help="heads per chunk of the host-buffer calls (0 = the library default, half of B*H)")
     ap.add_argument("--prefill-workload", default=PREFILL,
                     choices=["prefill_2k", "prefill_8k", "prefill_32k", "prefill_32k_pad"],
                     help="prefill workload of the step (default: the 2k / d=64 headline workload)")
@@ -613,7 +615,7 @@ def main():
         ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_e)]
         # the host-buffer entry point takes no key mask: no end-to-end leg for the padded workload
         if do_p and not wp.pad_heads:
-            te_p = e2e_prefill(fa, wp, modes, q, k, v, n_e, dev)
+            te_p = e2e_prefill(fa, wp, modes, q, k, v, n_e, dev, args.e2e_chunk_heads)
         if do_d:
             hdq = dq.cpu().pin_memory()
             hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
@@ -639,7 +641,7 @@ def main():
                    "d2h_bytes_per_step": nm * (o.numel() * 2 + lse.numel() * 4),
                    "steps": n_e,
                    "api": "fa_fwd_host (C ABI, host buffers), one call per causal mode",
-                   "chunk_heads": max(1, -(-wp.B * wp.H // 4)),
+                   "chunk_heads": args.e2e_chunk_heads or max(1, -(-wp.B * wp.H // 2)),
                    "note": "every call uploads q, k, v from pinned host memory in chunks of heads, runs the fused "
                            "kernel per chunk and reads o, lse back; copies and kernels of consecutive chunks "
                            "overlap inside the call; the two modes' calls are independent requests on one "

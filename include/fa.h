@@ -88,7 +88,7 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
 
 /* Bytes of device workspace fa_fwd_host needs: two buffer sets, each holding
  * q, k, v, o and lse of one chunk of heads (every region rounded up to 256
- * bytes). chunk_heads <= 0 selects the default, ceil(B*H / 4) heads. Returns 0
+ * bytes). chunk_heads <= 0 selects the default, ceil(B*H / 2) heads. Returns 0
  * for invalid arguments. */
 size_t fa_fwd_host_workspace_size(int B, int H, int Nq, int Nk, int d, int chunk_heads);
 

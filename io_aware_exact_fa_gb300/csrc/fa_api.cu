@@ -188,11 +188,12 @@ HostSet host_set_layout(long long ch, int Nq, int Nk, int d) {
   h.bytes = h.lse + up(static_cast<size_t>(ch) * Nq * 4);
   return h;
 }
-// Heads per chunk: the caller's choice, else a quarter of B*H. Fewer, larger
-// chunks keep every chunk's launch wide enough to fill the GPU; four still
-// let the uploads of one chunk overlap the kernel of the previous one.
+// Heads per chunk: the caller's choice, else half of B*H. Few, large chunks
+// keep every chunk's launch wide enough to fill the GPU; two still let one
+// chunk's uploads overlap the other's kernel, and consecutive calls on
+// different streams overlap each other.
 long long host_chunk_heads(long long BH, int chunk_heads) {
-  const long long ch = chunk_heads > 0 ? chunk_heads : (BH + 3) / 4;
+  const long long ch = chunk_heads > 0 ? chunk_heads : (BH + 1) / 2;
   return std::max(1LL, std::min(ch, BH));
 }
 

@@ -121,8 +121,8 @@ def test_fwd_host_workspace_and_validation(lib):
     ws.restype = ctypes.c_size_t
     ws.argtypes = [ctypes.c_int] * 6
     up = lambda x: (x + 255) // 256 * 256
-    # B=4 H=16 -> 64 heads, default chunk = 16 heads
-    q, kv, lse = up(16 * 2048 * 64 * 2), up(16 * 2048 * 64 * 2), up(16 * 2048 * 4)
+    # B=4 H=16 -> 64 heads, default chunk = 32 heads
+    q, kv, lse = up(32 * 2048 * 64 * 2), up(32 * 2048 * 64 * 2), up(32 * 2048 * 4)
     assert ws(4, 16, 2048, 2048, 64, 0) == 2 * (2 * q + 2 * kv + lse)
     assert ws(4, 16, 2048, 2048, 64, 1000) == ws(4, 16, 2048, 2048, 64, 64)  # clamped to B*H
     assert ws(1, 3, 100, 300, 128, 2) == 2 * (2 * up(2 * 100 * 256) + 2 * up(2 * 300 * 256) + up(2 * 100 * 4))
