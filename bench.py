@@ -194,6 +194,24 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "" if neither says."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return ""
+
+
 def oracle_prefill_sample(w, budget_s: float):
     """Time the fp64 oracle on whole heads of the prefill workload (non-causal
     and causal alternately) until ``budget_s`` is spent; returns (flops, seconds, heads)."""
@@ -457,7 +475,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
                    "causal": [False, True], "oracle": "oracle/attention.py attend_head"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "cpu": cpu_model(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -655,7 +673,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0 and do_p and args.prefill_workload == PREFILL:
         f, s, heads = oracle_prefill_sample(wp, args.cpu_budget)
-        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "cpu": cpu_model(), "kind": "oracle",
                "sample": f"{heads} whole heads (1 head = {wp.Nq}x{wp.Nk}, d={wp.d}) of {wp.name}, "
                          f"non-causal/causal alternating, fp64 NumPy, {s:.1f} s"}
 
