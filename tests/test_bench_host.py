@@ -93,7 +93,7 @@ def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     assert bench.recorded_traffic("decode_sm103.cu", "w_current") == 1234
     assert bench.recorded_traffic("decode_sm103.cu", "w_stale") is None     # kernel changed since the capture
     assert bench.recorded_traffic("decode_sm103.cu", "w_missing") is None
-    # a header the kernel includes is part of its hash
+    # each kernel source has its own hash (a record of one kernel never matches another)
     assert bench.kernel_hash("decode_grouped_sm103.cu") != bench.kernel_hash("decode_sm103.cu")
 
 
