@@ -28,7 +28,7 @@ constexpr int PREFILL_MMA_WARP0 = 9;       // warps 9, 10 issue MMAs (one per Q 
 // warpgroup, so 2 * SOFTMAX + PRODUCER must not exceed 3 * PREFILL_LAUNCH_REGS.
 constexpr int PREFILL_LAUNCH_REGS = 168;
 #ifndef FA_SOFTMAX_REGS_D64
-#define FA_SOFTMAX_REGS_D64 224
+#define FA_SOFTMAX_REGS_D64 216
 #endif
 #ifndef FA_SOFTMAX_REGS_D128
 #define FA_SOFTMAX_REGS_D128 216
