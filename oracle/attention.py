@@ -167,8 +167,8 @@ def online_attention_head(q, k, v, scale: float, causal: bool = False, keep=None
     [IO, "Executable recurrence, with an empty-state policy"]. After the last
     tile O = o / l (0 when l == 0) and lse = m + ln l (-inf when l == 0).
     """
-    if type(tile) is not int or tile <= 0:
-        raise ValueError("tile must be a positive integer")
+    if isinstance(tile, bool) or not isinstance(tile, int) or tile < 1:
+        raise ValueError(f"tile size {tile!r} is not an int of at least 1")
     q, k, v = _f64(q), _f64(k), _f64(v)
     Nq, Nk = q.shape[0], k.shape[0]
     rows = np.arange(Nq)
@@ -227,45 +227,55 @@ def online_attention(q, k, v, scale: float, causal: bool = False, keep=None,
 # Single-row forms, for the pages' worked examples
 # ---------------------------------------------------------------------------
 
-def _check_row_inputs(scores, values, tile):
-    """Input policy of the executable recurrence [IO, "Executable recurrence, ..."]:
-    one score per value row, a positive integer tile, finite values, and
-    scores that are finite or -inf (NaN and +inf are rejected)."""
-    s = np.asarray(scores, dtype=np.float64)
-    v = np.asarray(values, dtype=np.float64)
-    if v.ndim == 1:
-        v = v[:, None]
-    if s.ndim != 1 or v.ndim != 2 or s.shape[0] != v.shape[0]:
-        raise ValueError("one score per value row required")
-    if type(tile) is not int or tile <= 0:
-        raise ValueError("tile must be a positive integer")
-    if np.any(np.isnan(s) | np.isposinf(s)) or not np.all(np.isfinite(v)):
-        raise ValueError("values must be finite; scores finite or -inf")
-    return s, v
+def _row_arrays(scores, values, tile):
+    """One row's scores [N] and values [N] or [N, dv] as fp64 arrays (values
+    as [N, dv]), after the input policy that [IO, "Executable recurrence,
+    with an empty-state policy"] states: the counts must agree, the tile size
+    is a positive int, a score is finite or -inf (a masked key; NaN and +inf
+    are refused) and every value is finite. Anything else raises ValueError."""
+    sc = np.asarray(scores, dtype=np.float64)
+    vals = np.asarray(values, dtype=np.float64)
+    if vals.ndim == 1:
+        vals = vals.reshape(-1, 1)
+    if sc.ndim != 1 or vals.ndim != 2 or len(sc) != len(vals):
+        raise ValueError(f"{sc.shape} scores do not pair up with values of shape {vals.shape}")
+    if isinstance(tile, bool) or not isinstance(tile, int) or tile < 1:
+        raise ValueError(f"tile size {tile!r} is not an int of at least 1")
+    if np.isnan(sc).any() or (sc == np.inf).any():
+        raise ValueError("a score is NaN or +inf (allowed: finite, or -inf for a masked key)")
+    if not np.isfinite(vals).all():
+        raise ValueError("a value is NaN or infinite")
+    return sc, vals
 
 
 def online_row(scores, values, tile: int = 2, trace: bool = False):
     """One query row, new-max form [IO, "Keep only the state ..."; MEM, "Try it"].
 
     ``scores`` are already scaled and masked (-inf = masked); ``values`` is
-    [N] or [N, dv]. Returns the output vector (zeros for an empty or
-    all-masked row). With ``trace=True`` also returns the state (m, l, o,
-    alpha) after every tile that was folded in.
+    [N] or [N, dv]. The state after the keys folded in so far is the running
+    max m of their visible scores, l = sum exp(s_j - m) and
+    o = sum exp(s_j - m) v_j over them. Folding in one tile:
+        m' = max(m, scores of the tile),  alpha = exp(m - m'),
+        l' = alpha l + sum_tile w_j,  o' = alpha o + sum_tile w_j v_j,
+    with w_j = exp(s_j - m') for visible keys and 0 for masked ones. Before
+    any visible key m is -inf and l, o are 0; alpha is then taken as 0 (the
+    empty state has nothing to rescale). The output is o / l, or zeros when l
+    stays 0 (an empty or all-masked row). With ``trace=True`` the state
+    (m, l, o, alpha) after each tile is returned too.
     """
-    s, v = _check_row_inputs(scores, values, tile)
+    s, v = _row_arrays(scores, values, tile)
+    visible = ~np.isneginf(s)
     m, l = NEG_INF, 0.0
     o = np.zeros(v.shape[1])
     states = []
-    for start in range(0, s.shape[0], tile):
-        chunk = s[start:start + tile]
-        cmax = chunk.max()
-        if np.isneginf(cmax):           # all-masked chunk: nothing to fold in
-            continue
-        m_new = max(m, cmax)
-        alpha = 0.0 if np.isneginf(m) else math.exp(m - m_new)
-        w = np.exp(chunk - m_new)
-        l = alpha * l + w.sum()
-        o = alpha * o + w @ v[start:start + tile]
+    for t0 in range(0, len(s), tile):
+        idx = slice(t0, min(len(s), t0 + tile))
+        m_new = max(m, float(s[idx].max()))       # masked scores (-inf) never raise it
+        alpha = math.exp(m - m_new) if np.isfinite(m) else 0.0
+        base = m_new if np.isfinite(m_new) else 0.0
+        w = np.where(visible[idx], np.exp(s[idx] - base), 0.0)
+        l = alpha * l + float(w.sum())
+        o = alpha * o + w @ v[idx]
         m = m_new
         states.append(dict(m=m, l=l, o=o.copy(), alpha=alpha))
     out = o / l if l > 0 else np.zeros_like(o)
@@ -280,7 +290,7 @@ def blocklocal_row(scores, values, tile: int = 2, trace: bool = False):
     m_new with scale_old = exp(m_old - m_new) and scale_new =
     exp(m_block - m_new). Identical in exact arithmetic to ``online_row``.
     """
-    s, v = _check_row_inputs(scores, values, tile)
+    s, v = _row_arrays(scores, values, tile)
     m, l = NEG_INF, 0.0
     acc = np.zeros(v.shape[1])
     states = []

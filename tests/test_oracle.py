@@ -106,16 +106,19 @@ def pin_library(impl):
         q = rng.standard_normal((Nq, d))
         k = rng.standard_normal((Nk, d))
         v = rng.standard_normal((Nk, dv))
-        scale = 0.37
-        raw = scale * (q @ k.T)
         cases = [(False, None)]
         if Nq == Nk:
             cases.append((True, None))
         keep = rng.random((Nq, Nk)) < 0.5
         keep[np.arange(Nq), rng.integers(0, Nk, Nq)] = True   # no empty rows here
         cases.append((False, keep))
-        for causal, mask in cases:
-            ref = _sdpa(q, k, v, scale, causal, mask)
+        # a negative scale is a valid input of softmax(scale q k^T): the weights
+        # then favour the smallest dot products
+        for (causal, mask), scale in itertools.product(cases, (0.37, -0.6)):
+            raw = scale * (q @ k.T)
+            # torch's fp64 path takes the square root of its scale, so the
+            # negative case asks it for |scale| (q . -k) = scale (q . k), exactly
+            ref = _sdpa(q, np.sign(scale) * k, v, abs(scale), causal, mask)
             allowed = np.ones((Nq, Nk), bool) if mask is None else mask.copy()
             if causal:
                 allowed &= np.tril(np.ones((Nq, Nk), bool))
@@ -391,9 +394,11 @@ MUTANTS = [
      "ok &= (j - start) <= (rows[:, None] + (Nk - Nq))"),
     ("online: alpha sign", "alpha = np.where(np.isneginf(m), 0.0, np.exp(np.where(live, m - m_new, 0.0)))",
      "alpha = np.where(np.isneginf(m), 0.0, np.exp(np.where(live, m_new - m, 0.0)))"),
-    ("row: alpha sign", "alpha = 0.0 if np.isneginf(m) else math.exp(m - m_new)",
-     "alpha = 0.0 if np.isneginf(m) else math.exp(m_new - m)"),
-    ("row: dropped alpha on o", "o = alpha * o + w @ v[start:start + tile]", "o = o + w @ v[start:start + tile]"),
+    ("row: alpha sign", "alpha = math.exp(m - m_new) if np.isfinite(m) else 0.0",
+     "alpha = math.exp(m_new - m) if np.isfinite(m) else 0.0"),
+    ("row: dropped alpha on o", "o = alpha * o + w @ v[idx]", "o = o + w @ v[idx]"),
+    ("row: masked keys weighted", "w = np.where(visible[idx], np.exp(s[idx] - base), 0.0)",
+     "w = np.exp(np.where(visible[idx], s[idx], 0.0) - base)"),
     ("blocklocal: scale_new dropped", "scale_new = math.exp(m_block - m_new)", "scale_new = 1.0"),
     ("merge: weight sign", "w = np.where(live, np.exp(np.where(live, ms - M, 0.0)), 0.0)",
      "w = np.where(live, np.exp(np.where(live, M - ms, 0.0)), 0.0)"),
