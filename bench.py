@@ -116,8 +116,58 @@ def recorded_traffic(kernel_file: str, workload: str):
     return rec.get("dram_bytes_per_launch")
 
 
+# Clock sampler run as a separate process (no contention with the launching
+# thread): NVML through ctypes, one line per sample
+# "<unix time>,<sm MHz>,<max sm MHz>,<clock event reason bits>" every
+# <interval> ms. argv: device (a PCI bus id "dddddddd:bb:dd.f" or an NVML
+# index), interval in ms. Exits with status 3 if NVML cannot be used.
+NVML_SAMPLER = r"""
+import ctypes, sys, time
+try:
+    nv = ctypes.CDLL("libnvidia-ml.so.1")
+    assert nv.nvmlInit_v2() == 0
+    h = ctypes.c_void_p()
+    dev = sys.argv[1]
+    if ":" in dev:
+        assert nv.nvmlDeviceGetHandleByPciBusId_v2(dev.encode(), ctypes.byref(h)) == 0
+    else:
+        assert nv.nvmlDeviceGetHandleByIndex_v2(int(dev), ctypes.byref(h)) == 0
+    reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+        nv.nvmlDeviceGetCurrentClocksThrottleReasons
+    mx = ctypes.c_uint()
+    assert nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
+except Exception:
+    sys.exit(3)
+iv = float(sys.argv[2]) / 1000.0
+sm, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+out = sys.stdout
+while True:
+    t = time.time()
+    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and reasons_fn(h, ctypes.byref(rs)) == 0:
+        out.write("%.6f,%d,%d,%d\n" % (t, sm.value, mx.value, rs.value))
+        out.flush()
+    time.sleep(max(0.0, iv - (time.time() - t)))
+"""
+# NVML clock-event reason bits and the names reported for them
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+                0x80: "hw_power_brake_slowdown"}
+
+
+def nvml_device_id(index: int) -> str:
+    """The PCI bus id NVML knows the CUDA device `index` by (CUDA_VISIBLE_DEVICES
+    may renumber devices), or the index itself when torch does not say."""
+    try:
+        import torch
+        pr = torch.cuda.get_device_properties(index)
+        return "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+    except Exception:
+        return str(index)
+
+
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """Samples of the SM clock and the clock-event (throttle) reasons during
+    the timed regions: NVML every 2 ms from a separate process, else
+    nvidia-smi every 50 ms."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -129,9 +179,25 @@ class ClockSampler:
         self.proc = None
         self.t = None
         self.window = None
+        self.source = None
 
     def start(self):
         try:
+            self.proc = subprocess.Popen([sys.executable, "-c", NVML_SAMPLER, nvml_device_id(self.index), "2"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline()
+            if first:
+                self.source = "nvml, 2 ms"
+                self._add_nvml(first)
+                self.t = threading.Thread(target=self._read_nvml, daemon=True)
+                self.t.start()
+                return
+            self.proc.wait(timeout=5)
+        except (OSError, subprocess.SubprocessError):
+            pass
+        self.proc = None
+        try:
+            self.source = "nvidia-smi, 50 ms"
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
@@ -141,6 +207,20 @@ class ClockSampler:
             return
         self.t = threading.Thread(target=self._read, daemon=True)
         self.t.start()
+
+    def _add_nvml(self, line):
+        try:
+            t, sm, mx, bits = line.strip().split(",")
+            bits = int(bits)
+        except ValueError:
+            return
+        names = ["Active" if bits & b else "Not Active" for b in (0x8, 0x40, 0x20, 0x4)]
+        # same field order as the nvidia-smi rows: timestamp, sm, max, power, active, hw, hw_thermal, sw_thermal, sw_cap
+        self.samples.append((float(t), ["", sm, mx, "", str(bits)] + names))
+
+    def _read_nvml(self):
+        for line in self.proc.stdout:
+            self._add_nvml(line)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -166,7 +246,8 @@ class ClockSampler:
             return None
         rows = list(self.samples)
         if window:
-            inside = [r for r in rows if window[0] - 0.06 <= r[0] <= window[1] + 0.06]
+            pad = 0.004 if self.source and self.source.startswith("nvml") else 0.06
+            inside = [r for r in rows if window[0] - pad <= r[0] <= window[1] + pad]
             rows = inside or rows
         if not rows:
             return None
@@ -184,7 +265,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sampler": self.source}
 
 
 def cpu_cores():
@@ -450,6 +531,82 @@ def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
     return out
 
 
+LONG_CONTEXT = ("prefill_8k", "prefill_32k", "prefill_32k_pad")
+
+
+def run_long_context(args, fa, W, flush, stream, warm, world, rank, dev):
+    """Time the fused prefill on the long-context workloads (B=1 H=32 N=8192
+    d=128 causal; B=1 H=8 N=32768 d=128 causal, without and with key padding
+    on half the heads), one launch per step with its own CUDA events; then
+    the backward pass on the 8k workload. Their inputs (201 MB of q, k, v)
+    exceed L2; the L2 is flushed between steps anyway, outside the events."""
+    import torch
+    peaks = measured_peaks()
+    out = {"workloads": {}}
+    K = args.steps
+    for key in LONG_CONTEXT:
+        w = W.WORKLOADS[key]
+        q, k, v = W.make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, seed=rank, device="cuda")
+        o = torch.empty_like(q)
+        lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device=dev)
+        words, strides = None, (0, 0, 0)
+        if w.pad_heads:
+            wb = W.pack_keep_bits(W.key_padding_keep(w.B, w.H, w.Nk, w.pad_heads, w.pad_from))
+            words, strides = wb.to(dev), W.mask_strides(wb)
+        causal = w.causal_modes[0]
+
+        def call():
+            fa.fwd(q, k, v, scale=w.scale, causal=causal, keep_bits=words, mask_strides=strides, out=o, lse=lse)
+
+        for _ in range(warm):
+            flush.zero_()
+            call()
+        torch.cuda.synchronize()
+        if fa.device_status() != fa.FA_OK:
+            raise RuntimeError(f"device status not OK after the {w.name} warm-up")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        n0 = fa.launch_count()
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        t1 = time.time()
+        launches = fa.launch_count() - n0
+        if fa.device_status() != fa.FA_OK:
+            raise RuntimeError(f"device status not OK after the {w.name} timed region")
+        t = max_over_ranks([sum(a.elapsed_time(b) for a, b in ev) / 1e3], world, dev)[0]
+        f = w.flops(causal)
+        ach = K * f / t / 1e12
+        rec = {"value": whole_job_rate(f, K, t, world) / 1e12, "unit": "TFLOP/s", "ms": t / K * 1e3,
+               "gpu_launches": launches,
+               "config": {"B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "scale": w.scale, "causal": causal,
+                          "key_padding": ({"heads_below": w.pad_heads, "keys_from": w.pad_from}
+                                          if w.pad_heads else None)},
+               "roofline": {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": ach / peaks["bf16_tflops"],
+                            "traffic": recorded_traffic("prefill_sm103.cu", w.name),
+                            "kernel": f"fa_prefill_kernel<{w.d}>", "peak_source": f"{peaks['source']} bf16 burst",
+                            "flop_convention": "4*B*H*Nq*Nk*d, halved for causal (nominal: padded keys counted)"},
+               "_window": (t0, t1)}
+        if w.pad_heads:
+            share = visible_pair_fraction(w, causal)
+            rec["roofline"]["visible_pair_share"] = share
+            rec["roofline"]["tflops_effective"] = ach * share
+        if key == "prefill_8k" and not args.no_backward:
+            rec["backward"] = run_backward(args, fa, W, w, [causal], q, k, v, lse, flush, stream, warm, world, rank,
+                                           dev)
+        out["workloads"][w.name] = rec
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------- reference
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -493,7 +650,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for cpu_baseline (0 = skip)")
     ap.add_argument("--only", default="all",
-                    choices=["all", "prefill", "decode", "backward", "decode_variants", "materialized"],
+                    choices=["all", "prefill", "decode", "backward", "decode_variants", "materialized",
+                             "long_context"],
                     help="run one part of the step only (small profiling runs)")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the backward-pass leg (timed after the step, reported under 'backward')")
@@ -501,6 +659,8 @@ def main():
     ap.add_argument("--prefill-h", type=int, default=0, help="override the prefill heads (profiling a small case)")
     ap.add_argument("--dv-b", type=int, default=0, help="override the decode-variant batch (profiling a small case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the long-context prefill legs (8k and 32k, d=128; reported under 'long_context')")
     ap.add_argument("--e2e-chunk-heads", type=int, default=0,
                     help="heads per chunk of the host-buffer calls (0 = the library default, half of B*H)")
     ap.add_argument("--prefill-workload", default=PREFILL,
@@ -535,6 +695,8 @@ def main():
     do_b = args.only in ("all", "backward") and not args.no_backward and not wp.pad_heads
     do_v = args.only in ("all", "decode_variants")
     do_m = args.only in ("all", "materialized") and not wp.pad_heads
+    do_l = args.only in ("all", "long_context") and not args.no_long and args.prefill_workload == PREFILL \
+        and not args.prefill_h
     modes = list(wp.causal_modes)
     wd = W.WORKLOADS[DECODE]
     if args.decode_b:
@@ -607,6 +769,7 @@ def main():
     bwd = run_backward(args, fa, W, wp, modes, q, k, v, lse, flush, stream, warm, world, rank, dev) if do_b else None
     dvar = run_decode_variants(args, fa, W, stream, warm, world, rank, dev) if do_v else None
     mat = run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, dev) if do_m else None
+    lng = run_long_context(args, fa, W, flush, stream, warm, world, rank, dev) if do_l else None
     sampler.stop()
     clocks = sampler.summary((t_wall0, t_wall1))
     if bwd is not None:
@@ -615,6 +778,11 @@ def main():
         dvar["clocks"] = sampler.summary(dvar.pop("_window"))
     if mat is not None:
         mat["clocks"] = sampler.summary(mat.pop("_window"))
+    if lng is not None:
+        for rec in lng["workloads"].values():
+            rec["clocks"] = sampler.summary(rec.pop("_window"))
+            if "backward" in rec:
+                rec["backward"]["clocks"] = sampler.summary(rec["backward"].pop("_window"))
 
     nm = len(modes)
     t_modes = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / 1e3 for i in range(nm)]
@@ -746,6 +914,11 @@ def main():
             mat["fused_speedup"] = {("causal" if c else "noncausal"): tmm / tm
                                     for c, tm, tmm in zip(modes, t_modes, t_mat)}
         line["materialized"] = mat
+    if lng is not None:
+        line["long_context"] = lng
+        if not do_p and not do_d and bwd is None and dvar is None:
+            first = next(iter(lng["workloads"].values()))
+            line["value"], line["unit"] = first["value"], "TFLOP/s"
     if dvar is not None:
         line["decode_variants"] = dvar
         if not do_p and not do_d and bwd is None:

@@ -31,7 +31,9 @@
  *             holds ceil(Nk / 32) words; bits past Nk are ignored.
  *   stream    a cudaStream_t (NULL = the legacy default stream).
  * Supported: d in {64, 128}; q, k, v, o 16-byte aligned; keep_bits 4-byte
- * aligned; 1 <= B*H, Nk < 2^31; scale finite and >= 0.
+ * aligned; 1 <= B*H, Nk < 2^31; scale any finite value (a negative scale
+ * gives the largest weights to the smallest dot products, as the definition
+ * says; scale 0 gives uniform weights over the visible keys).
  *
  * Ownership: the caller allocates and owns every buffer; the library keeps
  * no pointer after a call returns and allocates no device memory per call
@@ -41,8 +43,8 @@
  * Errors (checked on the host before anything is launched; nothing is
  * written on error):
  *   FA_ERR_INVALID_ARG  a required pointer is NULL, a size is negative or
- *                       zero where it must be positive, scale is NaN/inf or
- *                       negative, or a size overflows the supported range.
+ *                       zero where it must be positive, scale is NaN or
+ *                       infinite, or a size overflows the supported range.
  *   FA_ERR_UNSUPPORTED  d not in {64, 128}, a misaligned pointer, or no
  *                       sm_103 device is current. There is no fallback path.
  *   FA_ERR_WORKSPACE    the decode workspace is NULL or too small.
@@ -52,6 +54,11 @@
  *                       undefined, the CUDA context stays usable.
  * Inputs are not scanned for NaN/inf (that would cost bandwidth): a NaN or
  * inf in q, k or v propagates to the rows it touches.
+ *
+ * Device reset: the first call on a device caches that device's state (the
+ * status word's address, kernel attributes, the no-alloc scratch address)
+ * for its primary context. cudaDeviceReset while the library is loaded
+ * invalidates that state; calls made after a reset are not supported.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -160,7 +167,9 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
  *     nothing; use fa_decode_splitkv with a caller workspace instead.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is cached for the device's
+ *     primary context; after cudaDeviceReset it is stale, as is the rest of
+ *     the library's per-device state (see "Device reset" above).
  *   - All calls share the one array: calls whose work overlaps on the GPU
  *     (different streams, or host threads without ordering) race and corrupt
  *     each other's results. Calls ordered on one stream are safe; the array
@@ -244,7 +253,7 @@ size_t fa_bwd_workspace_size(int B, int H, int Nq, int d);
  *   workspace       device memory of at least fa_bwd_workspace_size() bytes,
  *                   256-byte aligned, owned by the caller; overwritten.
  * Requires B, H, Nq, Nk >= 1, d in {64, 128}, 16-byte aligned bf16 buffers,
- * a finite scale >= 0. Keys no visible query reaches get dk = dv = 0. Three
+ * a finite scale. Keys no visible query reaches get dk = dv = 0. Three
  * launches on `stream` (statistics, the fused tiles, dq conversion); errors
  * as for fa_fwd, plus FA_ERR_WORKSPACE. */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

@@ -16,7 +16,8 @@ struct DecodeGroupedParams {
   int B, H, Hkv, G, Nq, R;   // G = H / Hkv query heads per K/V head; R = G * Nq rows per tile
   int Nk;                    // keys in the cache per (b, kv head)
   int S, chunk;              // splits; keys per split (a multiple of 128)
-  float scale_log2;          // scale * log2(e)
+  float scale_log2;          // |scale| * log2(e)
+  int negate_s;              // scale < 0: the score MMA computes -(Q K^T)
   uint64_t wait_limit_ns;
   unsigned int* status;      // device status word
 };

@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
     };
     constexpr uint32_t DHI = sdesc_sw128_hi(1024);
     const uint32_t q_lo = sdesc_sw128_lo(smem_u32(sQ), 16);
+    const uint32_t idesc_s = C::IDESC_S | (p.negate_s ? IDESC_NEGATE_A : 0u);
     // K-major K-step kk of a tile: (kk / 4) boxes plus (kk % 4) x 32 bytes in;
     // MN-major K-step kk: 16 rows = 2048 bytes in (64-column boxes BOX apart)
     auto kmaj = [](int kk) { return static_cast<uint32_t>(((kk >> 2) * C::BOX + (kk & 3) * 32) >> 4); };
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_w(tS, q_lo + kmaj(kk), DHI, k_lo + kmaj(kk), DHI, C::IDESC_S, kk > 0 ? 1u : 0u);
+          mma_ss_w(tS, q_lo + kmaj(kk), DHI, k_lo + kmaj(kk), DHI, idesc_s, kk > 0 ? 1u : 0u);
         mma_commit(s_full + (j & 1));
       }
     };
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
         sv[c] = __float_as_uint(x);
         mx = fmaxf(mx, x);
       }
-      const float mx2 = mx * sl2;  // log2 units (-inf stays -inf: scale_log2 > 0)
+      const float mx2 = mx * sl2;  // log2 units (-inf stays -inf: scale_log2 > 0, the sign is in the MMA)
       // move the reference max only when this tile's max exceeds it by more than the threshold
       const bool move = mx2 > m_ref + DG_RESCALE_THRESHOLD;
       float alpha = 1.f;

@@ -274,16 +274,18 @@ namespace {
 static __device__ __align__(256) unsigned char g_decode_scratch[FA_DECODE_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {nullptr};
+void* g_scratch_ptr[fa::kMaxDevices] = {nullptr};
 
 // Per-device set-up, done by the first call on each device (with that device
 // current): the array's name is only a host-side stand-in, so its device
-// address is looked up and cached.
+// address is looked up and cached. Like the rest of the library's per-device
+// state, the cached address belongs to the device's primary context as it
+// was at that first call; it is not valid after cudaDeviceReset.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= fa::kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;

@@ -53,7 +53,7 @@ struct DeviceState {
   unsigned int* status = nullptr;
   int num_sms = 0;
 };
-constexpr int kMaxDevices = 64;
+using fa::kMaxDevices;
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -132,7 +132,7 @@ fa_status encode_map(CUtensorMap* map, const void* base, int rows, int BH, int d
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 fa_status check_scale(float scale) {
-  if (!std::isfinite(scale) || scale < 0.f) return fail(FA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
   return FA_OK;
 }
 
@@ -268,10 +268,14 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
   p.Nk = Nk;
   p.n_qpairs = static_cast<int>(n_qpairs);
   p.causal = causal ? 1 : 0;
-  // scale 0 (uniform weights) runs with the smallest normal multiplier instead,
-  // so masked scores (-inf) still map to -inf and exponentiate to exactly 0;
-  // every weight then differs from 1 by far less than fp32 resolution.
-  p.scale_log2 = fmaxf(scale * 1.4426950408889634f, 1.17549435e-38f);
+  // A negative scale runs as |scale| times the negated scores (the score MMA
+  // negates Q), so the row maximum is taken where the weights are largest.
+  // Scale 0 (uniform weights) runs with the smallest normal multiplier
+  // instead, so masked scores (-inf) still map to -inf and exponentiate to
+  // exactly 0; every weight then differs from 1 by far less than fp32
+  // resolution.
+  p.scale_log2 = fmaxf(fabsf(scale) * 1.4426950408889634f, 1.17549435e-38f);
+  p.negate_s = scale < 0.f ? 1 : 0;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
   p.max_ctas = st->num_sms;
@@ -497,7 +501,9 @@ fa_status fa_decode_grouped(const void* q, const void* k_cache, const void* v_ca
   p.Nk = Nk;
   p.S = num_splits;
   p.chunk = ((Nk + num_splits - 1) / num_splits + 127) / 128 * 128;
-  p.scale_log2 = fmaxf(scale * 1.4426950408889634f, 1.17549435e-38f);
+  // as in the prefill: a negative scale negates the scores in the MMA
+  p.scale_log2 = fmaxf(fabsf(scale) * 1.4426950408889634f, 1.17549435e-38f);
+  p.negate_s = scale < 0.f ? 1 : 0;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -684,8 +690,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.Nk = Nk;
   p.causal = causal ? 1 : 0;
   p.scale = scale;
-  // as in the forward pass, scale 0 runs with the smallest normal multiplier
-  p.scale_log2 = fmaxf(scale * 1.4426950408889634f, 1.17549435e-38f);
+  // as in the forward pass, scale 0 runs with the smallest normal multiplier;
+  // the backward pass takes no row maximum, so a negative scale keeps its sign
+  p.scale_log2 = scale == 0.f ? 1.17549435e-38f : scale * 1.4426950408889634f;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
   cudaError_t e = fa::launch_bwd(d, tq, tk, tv, tdo, p, o, dout, lse, dq, static_cast<cudaStream_t>(stream));

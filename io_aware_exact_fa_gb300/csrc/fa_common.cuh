@@ -14,15 +14,16 @@ namespace fa {
 // fa_get_device_status).
 constexpr unsigned int FA_DEV_TIMEOUT = 1u;   // a bounded wait ran out
 
+// Device ordinals the host side keeps per-device state for (0 .. kMaxDevices-1).
+constexpr int kMaxDevices = 64;
+
 // Prefill tiling: 128 query rows per Q tile, two Q tiles per CTA, 128 keys per
 // K/V tile.
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_N = 128;
 constexpr int Q_TILES = 2;
 constexpr int PREFILL_THREADS = 384;       // 2 softmax warpgroups + 1 producer warpgroup
-constexpr int PREFILL_SOFTMAX_WARPS = 8;   // warps 0-3: Q tile 0, warps 4-7: Q tile 1
-constexpr int PREFILL_TMA_WARP = 8;
-constexpr int PREFILL_MMA_WARP0 = 9;       // warps 9, 10 issue MMAs (one per Q tile); 11 idle
+constexpr int PREFILL_SOFTMAX_WARPS = 8;   // warps 0-3: Q tile 0, warps 4-7: Q tile 1; 8-11 producers
 // Register split after set-up (setmaxnreg): the launch gives every thread
 // PREFILL_LAUNCH_REGS; each SM sub-partition holds one warp of every
 // warpgroup, so 2 * SOFTMAX + PRODUCER must not exceed 3 * PREFILL_LAUNCH_REGS.
@@ -58,7 +59,8 @@ struct PrefillParams {
   int B, H, Nq, Nk;
   int n_qpairs;              // ceil(Nq / 256)
   int causal;
-  float scale_log2;          // scale * log2(e)
+  float scale_log2;          // |scale| * log2(e)
+  int negate_s;              // scale < 0: the score MMA computes -(Q K^T)
   uint64_t wait_limit_ns;
   unsigned int* status;      // device status word
   int max_ctas;              // CTAs of a persistent launch (the SM count)

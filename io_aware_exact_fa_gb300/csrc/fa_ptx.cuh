@@ -188,6 +188,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Bit 13 of the kind::f16 instruction descriptor negates A: with it the
+// product is -(A B^T). A negative softmax scale is run as |scale| times the
+// negated scores, so that every kernel's row maximum is still taken over
+// scores that grow with the weights.
+constexpr uint32_t IDESC_NEGATE_A = 1u << 13;
+
 // D[tmem] (+)= A[smem] * B[smem]^T   (one elected thread issues)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {

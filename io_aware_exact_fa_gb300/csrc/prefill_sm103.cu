@@ -18,12 +18,15 @@
 // across units, so the next unit's loads and first MMAs overlap the current
 // unit's last steps and epilogue.
 // 384 threads = 3 warpgroups; after set-up the softmax warpgroups take more
-// registers and the producer warpgroup fewer (setmaxnreg).
+// registers and the producer warpgroup fewer (setmaxnreg). The producer
+// warpgroup is warps 8-11; within it:
 //   warp 8      TMA producer for K_j / V_j, into separate rings of slots.
 //   warp 9      TMEM allocator; with warp 10, MMA issuers (one per Q tile):
-//               S_t = Q_t K_j^T into TMEM, later O_t += P_t V_j.
+//               S_t = Q_t K_j^T into TMEM, later O_t += P_t V_j. (With
+//               FA_SINGLE_ISSUE_D64, lane 0 of warp 9 issues for both.)
 //   warp 11     TMA producer for Q (one tile per buffer per unit).
-//   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1: each thread
+//   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1 (warp w reads
+//               TMEM lanes 32 (w % 4) ..): each thread
 //               owns one query row (TMEM lane), reads its 128 scores with
 //               tcgen05.ld, applies the mask from absolute positions, folds
 //               the tile into (m, l), writes P (bf16) to TMEM and rescales
@@ -85,6 +88,9 @@ namespace fa {
 #ifndef FA_SOLO_ISSUE_D128
 #define FA_SOLO_ISSUE_D128 0
 #endif
+#ifndef FA_SINGLE_ISSUE_D64
+#define FA_SINGLE_ISSUE_D64 0    // one thread issues both Q tiles' MMAs, whichever is ready (else one warp per tile)
+#endif
 #ifndef FA_STAGGER_MIN_TILES
 #define FA_STAGGER_MIN_TILES 8   // only units this long amortise the delayed start
 #endif
@@ -142,6 +148,9 @@ struct PrefillCfg {
   // walks the issue loop: its waits then need no warp vote, and lanes 1-31
   // wait once, at the end, for the drain.
   static constexpr bool SOLO_ISSUE = (D == 64) ? FA_SOLO_ISSUE_D64 : FA_SOLO_ISSUE_D128;
+  // One issuing thread for both Q tiles (separate P columns only): it keeps
+  // each tile's next product in view and issues whichever is ready.
+  static constexpr bool SINGLE_ISSUE = SEP_P && FA_SINGLE_ISSUE_D64;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -297,6 +306,14 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Roles by warpgroup: the two softmax warpgroups (warps 0-7) and the
+  // producer warpgroup (K/V TMA, MMA issuers, Q TMA); pw is a warp's index
+  // within the producer warpgroup. (The producer warpgroup placed first, at
+  // warps 0-3, measured 2-3 % slower.)
+  const bool producer = warp >= PREFILL_SOFTMAX_WARPS;
+  const int pw = warp - PREFILL_SOFTMAX_WARPS;
+  const int sw = warp;
+  const bool alloc_warp = producer && pw == 1;  // the first MMA issuer allocates and frees TMEM
   const uint64_t lim = p.wait_limit_ns;
   const int U = p.units;
   const int G = static_cast<int>(gridDim.x);
@@ -307,7 +324,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   // launches one CTA per unit and warp 11 finds that tile before set-up ends.
   const bool trim = p.keep != nullptr && p.msq == 0;
 
-  if (trim && warp == PREFILL_SOFTMAX_WARPS + 3) {
+  if (trim && producer && pw == 3) {
     const int bh = cta % (p.B * p.H);
     const int b = bh / p.H, h = bh % p.H;
     const uint32_t* kb = p.keep + b * p.msb + h * p.msh;
@@ -331,13 +348,13 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     }
     for (int i = 0; i < NK; ++i) mbar_init(full_k + i, 1);
     for (int i = 0; i < NV; ++i) mbar_init(full_v + i, 1);
-    for (int i = 0; i < NR; ++i) mbar_init(rel + i, Q_TILES);  // both MMA-issuing warps
+    for (int i = 0; i < NR; ++i) mbar_init(rel + i, C::SINGLE_ISSUE ? 1 : Q_TILES);  // each MMA issuer
     mbar_init(unit_done, Q_TILES);
     mbar_init(drain, Q_TILES);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == PREFILL_MMA_WARP0) {
+  if (alloc_warp) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -350,10 +367,10 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   // units (counts of units, key tiles and per-tile steps done so far).
   auto unit_at = [&](int k) { return unit_of(cta, k, G, snake); };
 
-  if (warp >= PREFILL_SOFTMAX_WARPS) {
+  if (producer) {
     setmaxnreg_dec<prefill_producer_regs(D)>();
     const bool leader = lane == 0;
-    if (warp == PREFILL_TMA_WARP) {
+    if (pw == 0) {
       // ------------------------------------------------------ K/V TMA producer
       // The whole warp runs the loop and waits; lane 0 issues the copies.
       // Key tile g (counted over all units of this CTA) goes to K slot g % NK
@@ -401,7 +418,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         for (int n = max(0, nlv - NV); n < nlv; ++n) mbar_wait_drain(full_v + (n % NV), (n / NV) & 1, lim);
       }
       __syncwarp();
-    } else if (warp == PREFILL_SOFTMAX_WARPS + 3) {
+    } else if (pw == 3) {
       // ------------------------------------------------------- Q TMA producer
       // Q_t of unit k goes into its buffer once unit k-1 is done with it
       // (q_free_t, phase k-1) and Q_t of unit k-1 has landed (q_full_t).
@@ -439,7 +456,162 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           if (issued[t] > 0) mbar_wait_drain(q_full + t, (issued[t] - 1) & 1, lim);
       }
       __syncwarp();
-    } else if (warp == PREFILL_MMA_WARP0 || warp == PREFILL_MMA_WARP0 + 1) {
+    } else if (C::SINGLE_ISSUE) {
+      // ------------------------------------------------------ single MMA issuer
+      // Lane 0 of the first MMA warp issues every product of both Q tiles.
+      // tcgen05.mma issue runs only about one instruction ahead of the
+      // tensor pipe, so the issuer never blocks on one tile while the other
+      // has a product ready: it polls both tiles' next products
+      // (non-blocking) and issues the first one whose inputs are ready,
+      // trying the tile it did not serve last first.
+      // Per tile t and unit, with n key tiles, the products come in the
+      // order S_0, S_1, PV_0, S_2, PV_1, ..., PV_{n-1}: S_{j+1} may go as soon
+      // as the softmax has read S_j (s_free), PV_j once P_j is stored (p_full).
+      // Each tile walks the CTA's units on its own; a key tile is released
+      // (rel, one commit) once both tiles have issued every product that
+      // reads it, or have passed the unit that holds it.
+      if (pw == 1 && lane == 0) {
+        constexpr uint32_t DHI = sdesc_sw128_hi(1024);
+        const uint32_t k_lo = sdesc_sw128_lo(smem_u32(sK), 16);
+        const uint32_t v_lo = sdesc_sw128_lo(smem_u32(sV), C::BOX_BYTES);
+        const uint32_t idesc_s = C::IDESC_S | (p.negate_s ? IDESC_NEGATE_A : 0u);
+        struct TileState {
+          int k;        // unit (index in this CTA's sequence)
+          int n, nmax;  // key tiles of this tile / of the unit
+          int g0;       // ring position of the unit's first key tile
+          int c;        // this tile's steps in earlier units (barrier phases)
+          int ns, npv;  // S / PV products issued in this unit
+          bool live;    // the unit exists
+        };
+        TileState ts[Q_TILES];
+        auto enter = [&](TileState& x, int t, int k, int g0, int c) {
+          x.k = k;
+          x.g0 = g0;
+          x.c = c;
+          x.ns = 0;
+          x.npv = 0;
+          const int u = unit_at(k);
+          x.live = u < U;
+          if (x.live) {
+            const Unit w = unit_info(p, u, kv_keep);
+            x.n = t ? w.n1 : w.n0;
+            x.nmax = max(w.n0, w.n1);
+          } else {
+            x.n = x.nmax = 0;
+          }
+        };
+        enter(ts[0], 0, 0, 0, 0);
+        enter(ts[1], 1, 0, 0, 0);
+        bool issued_any = false;
+        bool ok = true;
+        int released = 0;  // key tiles below this ring position are released
+        // ring position below which tile t has issued every product it needs
+        auto done_pos = [&](const TileState& x) { return x.live ? x.g0 + x.npv : INT_MAX; };
+        // Tries to issue tile t's next product; returns true if it did (or
+        // if it moved the tile to its next unit).
+        auto try_tile = [&](int t) -> bool {
+          TileState& x = ts[t];
+          if (!x.live) return false;
+          if (x.ns == x.n && x.npv == x.n) {
+            // unit finished for this tile. A tile without key tiles releases
+            // its Q buffer once its Q load has landed (the Q producer then
+            // loads the next unit's Q into it).
+            if (x.n == 0 && C::O_STAGE) {
+              if (!mbar_test(smem_u32(q_full + t), x.k & 1)) return false;
+              mbar_arrive(q_free + t);
+            }
+            enter(x, t, x.k + 1, x.g0 + x.nmax, x.c + x.n);
+            return true;
+          }
+          if (x.ns < x.n && x.ns <= x.npv + 1) {
+            const int j = x.ns;
+            const int g = x.g0 + j;
+            const int cc = x.c + j;
+            bool rdy = mbar_test(smem_u32(full_k + (g % NK)), (g / NK) & 1);
+            if (rdy && cc > 0) rdy = mbar_test(smem_u32(s_free + t), (cc - 1) & 1);
+            if (rdy && j == 0) rdy = mbar_test(smem_u32(q_full + t), x.k & 1);
+            if (rdy) {
+              tc_fence_after();
+              const uint32_t q_lo = sdesc_sw128_lo(smem_u32(sQ) + t * C::TILE_BYTES, 16);
+              const uint32_t kb = k_lo + static_cast<uint32_t>(((g % NK) * C::TILE_BYTES) >> 4);
+              const uint32_t dS = tmem + BLOCK_N * t;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+                mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(s_full + t);
+              if (j == x.n - 1 && C::O_STAGE) mma_commit(q_free + t);  // Q_t read by its last S
+              issued_any = true;
+              ++x.ns;
+              return true;
+            }
+          }
+          if (x.npv < x.ns) {
+            const int j = x.npv;
+            const int g = x.g0 + j;
+            const int cc = x.c + j;
+            bool rdy = mbar_test(smem_u32(p_full + t), cc & 1);
+            if (rdy) rdy = mbar_test(smem_u32(full_v + (g % NV)), (g / NV) & 1);
+            if (rdy) {
+              tc_fence_after();
+              const uint32_t vb = v_lo + static_cast<uint32_t>(((g % NV) * C::TILE_BYTES) >> 4);
+              const uint32_t dO = tmem + C::O_COL + D * t;
+              const uint32_t aP = tmem + C::P_COL + C::P_STRIDE * t;
+#pragma unroll
+              for (int kk = 0; kk < BLOCK_N / 16; ++kk)
+                mma_ts_w(dO, aP + kk * 8, vb + kk * (2048 >> 4), DHI, C::IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(o_done + t);
+              issued_any = true;
+              ++x.npv;
+              return true;
+            }
+          }
+          return false;
+        };
+        int pref = 0;
+        uint64_t idle_t0 = 0;
+        uint32_t idle_n = 0;
+        while (ts[0].live || ts[1].live) {
+          bool moved = try_tile(pref);
+          if (moved) {
+            pref ^= 1;
+          } else {
+            moved = try_tile(pref ^ 1);
+          }
+          // release the key tiles both tiles are done with
+          const int rel_to = min(done_pos(ts[0]), done_pos(ts[1]));
+          for (; released < rel_to && released < INT_MAX; ++released) {
+            if (!ts[0].live && !ts[1].live) break;  // nothing loaded past the last unit
+            if (issued_any) mma_commit(rel + (released % NR));
+            else mbar_arrive(rel + (released % NR));
+          }
+          if (moved) {
+            idle_n = 0;
+            continue;
+          }
+          // nothing ready: bounded idle spell
+          if (idle_n == 0) idle_t0 = globaltimer_ns();
+          if ((++idle_n & 31u) == 0u) {
+            if (*abort_flag) { ok = false; break; }
+            if (globaltimer_ns() - idle_t0 > lim) {
+              *abort_flag = 1;
+              atomicOr(p.status, FA_DEV_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+        }
+        (void)ok;
+        if (issued_any) mma_commit(drain);
+        else mbar_arrive(drain);
+        mbar_wait_drain(drain, 0, lim);
+      } else if (lane == 0) {
+        mbar_arrive(drain);
+        mbar_wait_drain(drain, 0, lim);
+      }
+      __syncwarp();
+    } else {
       // ---------------------------------------------------------- MMA issuers
       // One warp per Q tile (tile 0 first). tcgen05.mma issue only runs about
       // one instruction ahead of the tensor pipe, so every barrier wait or
@@ -447,7 +619,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       // issuers each one's waits overlap the other's MMAs. Lane 0 issues the
       // MMAs and commits; with SOLO_ISSUE it also runs the loop alone,
       // otherwise the whole warp runs it and votes on every wait.
-      const int t = warp - PREFILL_MMA_WARP0;
+      const int t = pw - 1;
       const uint32_t sQa = smem_u32(sQ) + t * C::TILE_BYTES;
       // Low descriptor words of Q_t, K slot 0 and V slot 0 (every operand
       // shares the high word: 1024-byte 8-row groups, 128-byte swizzle). The
@@ -461,6 +633,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       const uint32_t dS = tmem + BLOCK_N * t;
       const uint32_t dO = tmem + C::O_COL + D * t;
       const uint32_t aP = tmem + C::P_COL + C::P_STRIDE * t;
+      const uint32_t idesc_s = C::IDESC_S | (p.negate_s ? IDESC_NEGATE_A : 0u);
       bool ok = true;
       bool issued_any = false;
 
@@ -520,7 +693,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-              mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, C::IDESC_S, kk > 0 ? 1u : 0u);
+              mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
             }
             mma_commit(s_full + t);
             // the unit's last score MMA: Q_t is free once it (and all before it)
@@ -646,8 +819,8 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   } else {
     setmaxnreg_inc<prefill_softmax_regs(D)>();
     // ------------------------------------------------- softmax / correction
-    const int t = warp >> 2;
-    const int wq = warp & 3;
+    const int t = sw >> 2;
+    const int wq = sw & 3;  // = warp % 4: the TMEM lane quarter this warp may access
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + BLOCK_N * t;
@@ -877,7 +1050,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == PREFILL_MMA_WARP0) {
+  if (alloc_warp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }

@@ -88,7 +88,6 @@ def test_host_validation_before_launch(lib):
     assert f(P, P, P, P, None, 1, 1, 8, 0, 64, 0.125, 0, None) == 1             # Nk = 0
     assert f(P, P, P, P, None, 1, 1, 8, 8, 64, float("nan"), 0, None) == 1      # scale NaN
     assert f(P, P, P, P, None, 1, 1, 8, 8, 64, float("inf"), 0, None) == 1      # scale inf
-    assert f(P, P, P, P, None, 1, 1, 8, 8, 64, -0.5, 0, None) == 1              # scale < 0
     assert f(P, P, P, P, None, 1, 1, 8, 8, 96, 0.125, 0, None) == 2             # d = 96
     assert f(P + 8, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, None) == 2         # misaligned q
     assert b"aligned" in lib.fa_last_error_detail()
@@ -133,7 +132,7 @@ def test_fwd_host_workspace_and_validation(lib):
                                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p])
     P, big = 1 << 20, 1 << 30
     assert f(None, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, 0, P, big, None) == 1       # NULL q
-    assert f(P, P, P, P, None, 1, 1, 8, 8, 64, -1.0, 0, 0, P, big, None) == 1           # scale < 0
+    assert f(P, P, P, P, None, 1, 1, 8, 8, 64, float("nan"), 0, 0, P, big, None) == 1   # scale NaN
     assert f(P, P, P, P, None, 1, 1, 8, 8, 80, 0.125, 0, 0, P, big, None) == 2          # d = 80
     assert f(P, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, 0, None, big, None) == 5       # no workspace
     assert f(P, P, P, P, None, 1, 1, 8, 8, 64, 0.125, 0, 0, P, 64, None) == 5           # too small

@@ -11,12 +11,10 @@ This file is collected last on purpose.
 import ctypes
 import math
 
-import numpy as np
 import pytest
 import torch
 
 from io_aware_exact_fa_gb300 import workloads as W
-from tests.parity import compare, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -50,8 +48,9 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
             assert _noalloc(fa, q, k, v, o, lse, scale, S) == fa.FA_OK, fa.lib.fa_last_error_detail()
             torch.cuda.synchronize()
             assert fa.device_status() == fa.FA_OK
-            compare(to64(o).reshape(B * H, d), to64(lse).reshape(-1), to64(ref_o).reshape(B * H, d),
-                    to64(ref_l).reshape(-1), f"noalloc call {call + 1} {(B, H, Nk, d, S)}")
+            # the same kernels on the same bytes: the outputs must be bit-identical
+            assert torch.equal(o, ref_o), f"noalloc call {call + 1} {(B, H, Nk, d, S)}: o differs"
+            assert torch.equal(lse, ref_l), f"noalloc call {call + 1} {(B, H, Nk, d, S)}: lse differs"
 
 
 def test_noalloc_rejects_requests_beyond_the_static_scratch(lib):
