@@ -129,6 +129,28 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int = 0,
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
 
 
+E4M3_MAX = 448.0  # largest finite e4m3 magnitude
+
+
+def make_qkv_fp8(B: int, H: int, Nq: int, Nk: int, d: int, seed: int = 0, device: str = "cpu"):
+    """FP8 inputs: the fp32 N(0,1) draws of ``make_qkv`` (same seed, same
+    order q, k, v), each tensor quantized to e4m3 with one descale factor
+    amax / 448 (so its largest magnitude maps to the largest e4m3 value,
+    round-to-nearest-even by torch's float8_e4m3fn conversion). Returns
+    (q8, k8, v8) as uint8 code tensors and (descale_q, descale_k, descale_v)
+    as Python floats."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    out, ds = [], []
+    for n in (Nq, Nk, Nk):
+        x = torch.randn(B, H, n, d, generator=g, device=device, dtype=torch.float32)
+        amax = float(x.abs().max()) if x.numel() else 1.0
+        descale = amax / E4M3_MAX if amax > 0 else 1.0
+        out.append((x / descale).to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
+        ds.append(descale)
+    return tuple(out), tuple(ds)
+
+
 def add_row_offsets(q: torch.Tensor, k: torch.Tensor, scale: float,
                     rows: Sequence[int] = PR1_OFFSET_ROWS,
                     signs: Sequence[float] = PR1_OFFSET_SIGNS,

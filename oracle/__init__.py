@@ -22,6 +22,10 @@ Every function restates what the pages compute, in fp64, with NumPy:
   the backward pass: gradients of a loss through O with respect to Q, K and V
   (the chain rule through the definition, with the exact P).
 
+* ``fp8.attend_head_fp8`` -- exact attention on e4m3 inputs: the 8-bit codes
+  decoded field by field (``fp8.e4m3_decode``), times their descale factors,
+  fed to the fp64 definition (pinned in tests/test_oracle_fp8.py).
+
 Pins (tests/test_oracle.py): the pages' worked examples (tests/golden/),
 agreement with torch's fp64 ``scaled_dot_product_attention`` and with
 ``scipy.special.logsumexp``, closed forms (one key, uniform scores, two keys),
