@@ -93,6 +93,27 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
                         const uint32_t* keep_bits, int64_t mstride_b, int64_t mstride_h,
                         int64_t mstride_q, void* stream);
 
+/* Forward pass on FP8 inputs ("FlashAttention: Attention Is Limited by
+ * Memory, Not Math", section "FlashAttention 1, 2 and 3", lists FP8 support
+ * among FlashAttention-3's changes; the pages give no further detail).
+ *   q, k, v   e4m3 codes (one byte each: 1 sign, 4 exponent bits with bias
+ *             7, 3 mantissa bits; no infinities), layouts as for fa_fwd;
+ *             16-byte aligned.
+ *   descale_q, descale_k, descale_v
+ *             one fp32 factor per tensor: the real value of a code c of q is
+ *             e4m3(c) * descale_q (likewise k, v); finite and > 0.
+ *   o, lse    bf16 O and fp32 lse of exact attention on those real values,
+ *             softmax(scale * Q K^T + causal mask) V, as fa_fwd defines them.
+ * The score and value products run on the tensor cores in e4m3 with fp32
+ * accumulation; P is rounded to e4m3 (round to nearest even) before the P V
+ * product, which is this path's main error against the exact result.
+ * Supported: d = 128 (FA_ERR_UNSUPPORTED otherwise); no key mask. Errors as
+ * for fa_fwd, plus FA_ERR_INVALID_ARG for a descale that is not finite and
+ * positive, or a product scale * descale_q * descale_k that overflows. */
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Nq, int Nk, int d, float scale,
+                     float descale_q, float descale_k, float descale_v, int causal, void* stream);
+
 /* Bytes of device workspace fa_fwd_host needs: two buffer sets, each holding
  * q, k, v, o and lse of one chunk of heads (every region rounded up to 256
  * bytes). chunk_heads <= 0 selects the default, ceil(B*H / 2) heads. Returns 0

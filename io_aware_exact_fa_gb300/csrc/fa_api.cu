@@ -82,8 +82,11 @@ fa_status device_state(DeviceState** out) {
     if ((e = cudaGetSymbolAddress(&p, fa::g_device_status)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status)");
     st.status = static_cast<unsigned int*>(p);
-    if ((e = fa::prefill_set_attributes(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
-    if ((e = fa::prefill_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
+    if ((e = fa::prefill_set_attributes(64, false)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
+    if ((e = fa::prefill_set_attributes(128, false)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
+    if ((e = fa::prefill_set_attributes(128, true)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(e4m3 d=128)");
     if ((e = fa::bwd_set_attributes(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=64)");
     if ((e = fa::bwd_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=128)");
     if ((e = fa::materialized_set_attributes()) != cudaSuccess)
@@ -94,11 +97,13 @@ fa_status device_state(DeviceState** out) {
       return cuda_fail(e, "cudaFuncSetAttribute(grouped decode d=128)");
     // The in-kernel register split assumes this launch allocation; a
     // different one could make setmaxnreg.inc wait forever, so refuse.
-    for (int d : {64, 128}) {
-      const int regs = fa::prefill_num_regs(d);
-      if (regs != fa::PREFILL_LAUNCH_REGS)
-        return fail(FA_ERR_UNSUPPORTED, "prefill kernel (d=%d) built with %d registers, expected %d", d, regs,
-                    fa::PREFILL_LAUNCH_REGS);
+    for (int v = 0; v < 3; ++v) {
+      const int d = v == 0 ? 64 : 128;
+      const bool f8 = v == 2;
+      const int regs = fa::prefill_num_regs(d, f8);
+      if (regs != fa::prefill_launch_regs(d))
+        return fail(FA_ERR_UNSUPPORTED, "prefill kernel (d=%d%s) built with %d registers, expected %d", d,
+                    f8 ? ", e4m3" : "", regs, fa::prefill_launch_regs(d));
     }
     if (g_encode == nullptr) {
       void* fn = nullptr;
@@ -117,12 +122,16 @@ fa_status device_state(DeviceState** out) {
 // 3-D bf16 tensor map over [BH, rows, d] with 128-row x 64-column boxes and
 // 128-byte swizzle; rows past `rows` read as zeros (loads) or are not written
 // (stores).
-fa_status encode_map(CUtensorMap* map, const void* base, int rows, int BH, int d) {
+// 3-D tensor map over [BH, rows, d] with 128-byte-swizzled boxes of 128 rows
+// x 128 bytes: 64 bf16 elements, or (e4m3) 128 one-byte codes.
+fa_status encode_map(CUtensorMap* map, const void* base, int rows, int BH, int d, bool e4m3 = false) {
+  const cuuint64_t esz = e4m3 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz, static_cast<cuuint64_t>(rows) * d * esz};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+  CUresult r = g_encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
@@ -228,13 +237,27 @@ uint64_t fa_launch_count(void) { return t_launches; }
 void fa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
 uint64_t fa_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
 
-fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
-                        int Nk, int d, float scale, int causal, const uint32_t* keep_bits, int64_t mstride_b,
-                        int64_t mstride_h, int64_t mstride_q, void* stream) {
+namespace {
+// e4m3 inputs of fa_fwd_fp8: the descale factors of q, k and v
+struct E4m3Inputs {
+  bool on = false;
+  float dq = 1.f, dk = 1.f, dv = 1.f;
+};
+
+// The prefill launch behind fa_fwd_masked and fa_fwd_fp8.
+fa_status prefill_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                         int Nk, int d, float scale, int causal, const uint32_t* keep_bits, int64_t mstride_b,
+                         int64_t mstride_h, int64_t mstride_q, const E4m3Inputs& f8, void* stream) {
   t_detail[0] = 0;
   if (B < 1 || H < 1 || Nk < 1 || Nq < 0)
     return fail(FA_ERR_INVALID_ARG, "need B >= 1, H >= 1, Nk >= 1, Nq >= 0 (got %d %d %d %d)", B, H, Nk, Nq);
   if (fa_status s = check_scale(scale)) return s;
+  if (f8.on) {
+    for (float x : {f8.dq, f8.dk, f8.dv})
+      if (!std::isfinite(x) || !(x > 0.f)) return fail(FA_ERR_INVALID_ARG, "descale factors must be finite and > 0");
+    if (!std::isfinite(scale * f8.dq * f8.dk)) return fail(FA_ERR_INVALID_ARG, "scale * descale_q * descale_k overflows");
+    if (d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported for e4m3 inputs (128)", d);
+  }
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
   if (Nq == 0) return FA_OK;  // nothing to compute (an empty q may have a NULL data pointer)
   if (!q || !k || !v || !o) return fail(FA_ERR_INVALID_ARG, "q, k, v and o must be non-NULL");
@@ -250,10 +273,10 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
   DeviceState* st = nullptr;
   if (fa_status s = device_state(&st)) return s;
   CUtensorMap tq, tk, tv, to;
-  if (fa_status s = encode_map(&tq, q, Nq, static_cast<int>(BH), d)) return s;
+  if (fa_status s = encode_map(&tq, q, Nq, static_cast<int>(BH), d, f8.on)) return s;
   if (fa_status s = encode_map(&to, o, Nq, static_cast<int>(BH), d)) return s;
-  if (fa_status s = encode_map(&tk, k, Nk, static_cast<int>(BH), d)) return s;
-  if (fa_status s = encode_map(&tv, v, Nk, static_cast<int>(BH), d)) return s;
+  if (fa_status s = encode_map(&tk, k, Nk, static_cast<int>(BH), d, f8.on)) return s;
+  if (fa_status s = encode_map(&tv, v, Nk, static_cast<int>(BH), d, f8.on)) return s;
 
   fa::PrefillParams p{};
   p.o = o;
@@ -274,8 +297,11 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
   // instead, so masked scores (-inf) still map to -inf and exponentiate to
   // exactly 0; every weight then differs from 1 by far less than fp32
   // resolution.
-  p.scale_log2 = fmaxf(fabsf(scale) * 1.4426950408889634f, 1.17549435e-38f);
+  // e4m3 inputs: the scores the MMA returns are in units of the codes, so
+  // the q and k descales join the scale, and O / l takes the v descale.
+  p.scale_log2 = fmaxf(fabsf(scale) * f8.dq * f8.dk * 1.4426950408889634f, 1.17549435e-38f);
   p.negate_s = scale < 0.f ? 1 : 0;
+  p.o_scale = f8.dv;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
   p.max_ctas = st->num_sms;
@@ -292,10 +318,29 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
     p.split_from = static_cast<int>(split ? U - r : U);
     p.units = static_cast<int>(split ? U + r : U);
   }
-  cudaError_t e = fa::launch_prefill(d, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = fa::launch_prefill(d, f8.on, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   t_launches += 1;
   return FA_OK;
+}
+}  // namespace
+
+fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                        int Nk, int d, float scale, int causal, const uint32_t* keep_bits, int64_t mstride_b,
+                        int64_t mstride_h, int64_t mstride_q, void* stream) {
+  return prefill_common(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, keep_bits, mstride_b, mstride_h, mstride_q,
+                        E4m3Inputs{}, stream);
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                     int Nk, int d, float scale, float descale_q, float descale_k, float descale_v, int causal,
+                     void* stream) {
+  E4m3Inputs f8;
+  f8.on = true;
+  f8.dq = descale_q;
+  f8.dk = descale_k;
+  f8.dv = descale_v;
+  return prefill_common(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, nullptr, 0, 0, 0, f8, stream);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,

@@ -22,34 +22,47 @@ constexpr int kMaxDevices = 64;
 constexpr int BLOCK_M = 128;
 constexpr int BLOCK_N = 128;
 constexpr int Q_TILES = 2;
-constexpr int PREFILL_THREADS = 384;       // 2 softmax warpgroups + 1 producer warpgroup
-constexpr int PREFILL_SOFTMAX_WARPS = 8;   // warps 0-3: Q tile 0, warps 4-7: Q tile 1; 8-11 producers
+constexpr int PREFILL_SOFTMAX_WARPS = 8;   // warps 0-3: Q tile 0, warps 4-7: Q tile 1; then the producers
+// Two softmax warpgroups and one producer warpgroup (K/V TMA, two MMA
+// issuers, Q TMA) at both head dimensions.
+__host__ __device__ constexpr int prefill_warpgroups(int) { return 3; }
+__host__ __device__ constexpr int prefill_threads(int d) { return 128 * prefill_warpgroups(d); }
 // Register split after set-up (setmaxnreg): the launch gives every thread
-// PREFILL_LAUNCH_REGS; each SM sub-partition holds one warp of every
-// warpgroup, so 2 * SOFTMAX + PRODUCER must not exceed 3 * PREFILL_LAUNCH_REGS.
-constexpr int PREFILL_LAUNCH_REGS = 168;
+// prefill_launch_regs(d) (the whole register file over the CTA's threads);
+// each SM sub-partition holds one warp of every warpgroup, so
+// 2 * SOFTMAX + (warpgroups - 2) * PRODUCER must not exceed
+// warpgroups * LAUNCH.
+__host__ __device__ constexpr int prefill_launch_regs(int d) { return prefill_warpgroups(d) == 4 ? 128 : 168; }
 #ifndef FA_SOFTMAX_REGS_D64
 #define FA_SOFTMAX_REGS_D64 216
 #endif
 #ifndef FA_SOFTMAX_REGS_D128
 #define FA_SOFTMAX_REGS_D128 216
 #endif
-// registers of the softmax warpgroups and of the producer/MMA warpgroup after
-// setmaxnreg, per head dimension (the d = 128 MMA issuers keep more state)
+// registers of the softmax warpgroups and of the producer warpgroups after
+// setmaxnreg, per head dimension
 __host__ __device__ constexpr int prefill_softmax_regs(int d) {
   return d == 64 ? FA_SOFTMAX_REGS_D64 : FA_SOFTMAX_REGS_D128;
 }
 __host__ __device__ constexpr int prefill_producer_regs(int d) {
-  return 3 * PREFILL_LAUNCH_REGS - 2 * prefill_softmax_regs(d) < 256 ? 3 * PREFILL_LAUNCH_REGS - 2 * prefill_softmax_regs(d)
-                                                                      : 256;
+  return (prefill_warpgroups(d) * prefill_launch_regs(d) - 2 * prefill_softmax_regs(d)) / (prefill_warpgroups(d) - 2) /
+                     8 * 8 < 256
+             ? (prefill_warpgroups(d) * prefill_launch_regs(d) - 2 * prefill_softmax_regs(d)) /
+                   (prefill_warpgroups(d) - 2) / 8 * 8
+             : 256;
 }
-static_assert(2 * prefill_softmax_regs(64) + prefill_producer_regs(64) <= 3 * PREFILL_LAUNCH_REGS &&
-                  2 * prefill_softmax_regs(128) + prefill_producer_regs(128) <= 3 * PREFILL_LAUNCH_REGS,
+static_assert(2 * prefill_softmax_regs(64) + (prefill_warpgroups(64) - 2) * prefill_producer_regs(64) <=
+                      prefill_warpgroups(64) * prefill_launch_regs(64) &&
+                  2 * prefill_softmax_regs(128) + (prefill_warpgroups(128) - 2) * prefill_producer_regs(128) <=
+                      prefill_warpgroups(128) * prefill_launch_regs(128),
               "setmaxnreg split exceeds the launch allocation");
 static_assert(prefill_softmax_regs(64) % 8 == 0 && prefill_softmax_regs(128) % 8 == 0 &&
-                  prefill_producer_regs(64) % 8 == 0 && prefill_producer_regs(128) % 8 == 0 &&
-                  prefill_producer_regs(64) >= 24 && prefill_producer_regs(128) >= 24,
-              "setmaxnreg counts are multiples of 8 in [24, 256]");
+                  prefill_producer_regs(64) >= 24 && prefill_producer_regs(128) >= 24 &&
+                  prefill_softmax_regs(64) >= prefill_launch_regs(64) &&
+                  prefill_softmax_regs(128) >= prefill_launch_regs(128) &&
+                  prefill_producer_regs(64) <= prefill_launch_regs(64) &&
+                  prefill_producer_regs(128) <= prefill_launch_regs(128),
+              "setmaxnreg counts are multiples of 8 in [24, 256], softmax up and producers down");
 
 struct PrefillParams {
   void* o;                   // bf16 [B*H, Nq, d]
@@ -59,8 +72,9 @@ struct PrefillParams {
   int B, H, Nq, Nk;
   int n_qpairs;              // ceil(Nq / 256)
   int causal;
-  float scale_log2;          // |scale| * log2(e)
+  float scale_log2;          // |scale| * log2(e) (e4m3 inputs: times the q and k descales)
   int negate_s;              // scale < 0: the score MMA computes -(Q K^T)
+  float o_scale;             // multiplies O / l: the v descale of e4m3 inputs, else 1
   uint64_t wait_limit_ns;
   unsigned int* status;      // device status word
   int max_ctas;              // CTAs of a persistent launch (the SM count)
@@ -97,11 +111,12 @@ struct DecodeParams {
 };
 
 // Launchers (defined next to their kernels). Return a CUDA error code.
-cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+// f8: the e4m3-input instantiation (d = 128 only); otherwise bf16 inputs.
+cudaError_t launch_prefill(int d, bool f8, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream);
-size_t prefill_smem_bytes(int d);
-cudaError_t prefill_set_attributes(int d);
-int prefill_num_regs(int d);   // registers per thread the prefill kernel launches with
+size_t prefill_smem_bytes(int d, bool f8);
+cudaError_t prefill_set_attributes(int d, bool f8);
+int prefill_num_regs(int d, bool f8);   // registers per thread the prefill kernel launches with
 cudaError_t launch_decode(int d, const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, const void* o, const void* dout, const float* lse,

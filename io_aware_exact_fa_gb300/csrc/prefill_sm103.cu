@@ -22,8 +22,7 @@
 // warpgroup is warps 8-11; within it:
 //   warp 8      TMA producer for K_j / V_j, into separate rings of slots.
 //   warp 9      TMEM allocator; with warp 10, MMA issuers (one per Q tile):
-//               S_t = Q_t K_j^T into TMEM, later O_t += P_t V_j. (With
-//               FA_SINGLE_ISSUE_D64, lane 0 of warp 9 issues for both.)
+//               S_t = Q_t K_j^T into TMEM, later O_t += P_t V_j.
 //   warp 11     TMA producer for Q (one tile per buffer per unit).
 //   warps 0-3   softmax for Q tile 0, warps 4-7 for Q tile 1 (warp w reads
 //               TMEM lanes 32 (w % 4) ..): each thread
@@ -88,51 +87,65 @@ namespace fa {
 #ifndef FA_SOLO_ISSUE_D128
 #define FA_SOLO_ISSUE_D128 0
 #endif
-#ifndef FA_SINGLE_ISSUE_D64
-#define FA_SINGLE_ISSUE_D64 0    // one thread issues both Q tiles' MMAs, whichever is ready (else one warp per tile)
-#endif
 #ifndef FA_STAGGER_MIN_TILES
 #define FA_STAGGER_MIN_TILES 8   // only units this long amortise the delayed start
 #endif
 
-template <int D>
+// F8: q, k and v are e4m3 codes (kind::f8f6f4 products, P rounded to e4m3);
+// otherwise bf16 (kind::f16). O is bf16 either way.
+template <int D, bool F8 = false>
 struct PrefillCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
-  static constexpr int TILE_BYTES = BLOCK_N * D * 2;  // one Q, K or V tile (128 rows x D bf16)
-  static constexpr int BOX_BYTES = 128 * 128;         // one TMA box: 128 rows x 64 bf16
-  static constexpr int NBOX = D / 64;
+  static_assert(!F8 || D == 128, "the e4m3 path is built for d = 128");
+  static constexpr int ESZ = F8 ? 1 : 2;              // bytes per q, k, v element
+  static constexpr int TILE_BYTES = BLOCK_N * D * ESZ;  // one Q, K or V tile (128 rows x D elements)
+  static constexpr int BOX_BYTES = 128 * 128;         // one TMA box: 128 rows x 128 bytes
+  static constexpr int BOX_ELEMS = 128 / ESZ;         // elements per box row (64 bf16 or 128 e4m3)
+  static constexpr int NBOX = D / BOX_ELEMS;
+  static constexpr int O_TILE_BYTES = BLOCK_M * D * 2;  // one bf16 O tile
+  static constexpr int NBOX_O = D / 64;
+  // products: one K-step takes 32 bytes of every A and B row (16 bf16 or 32
+  // e4m3 elements); S = Q K^T has D * ESZ / 32 of them, O += P V has
+  // BLOCK_N * ESZ / 32 (each K-step of V is PV_KROWS rows of 128 bytes)
+  static constexpr int KSTEPS_S = D * ESZ / 32;
+  static constexpr int KSTEPS_PV = BLOCK_N * ESZ / 32;
+  static constexpr int PV_KROWS = 32 / ESZ;
   // K and V stream through separate rings. K_j is read only by S = Q K_j^T,
   // V_j only by the later O += P V_j, so the K ring runs ahead of the V ring:
   // K_{j+1} can land while P_j is still being computed. Both slots of key
   // tile j are released together, by one release barrier per tile that both
   // issuers signal once their MMAs reading tile j have completed.
-  static constexpr int NK = (D == 128) ? 3 : 4;       // K ring slots
-  static constexpr int NV = (D == 128) ? 2 : 4;       // V ring slots
+  static constexpr int NK = (D == 128 && !F8) ? 3 : 4;  // K ring slots
+  static constexpr int NV = (D == 128 && !F8) ? 2 : 4;  // V ring slots
   static constexpr int NR = NK > NV ? NK : NV;        // release barriers (tile j uses j % NR)
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_TILES * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + NK * TILE_BYTES;
   // At d = 64 the epilogue stages O in buffers of its own, so the next unit's
   // Q may be loaded as soon as this unit's score MMAs are done; at d = 128
-  // there is no room and O is staged in the Q buffer.
-  static constexpr bool O_STAGE = (D == 64) && FA_O_STAGE;
+  // there is no room and O is staged in the Q buffer. An e4m3 Q tile is
+  // half the size of the bf16 O tile, so that path always stages O apart.
+  static constexpr bool O_STAGE = ((D == 64) && FA_O_STAGE) || F8;
   static constexpr int O_OFF = V_OFF + NV * TILE_BYTES;
-  static constexpr int BAR_OFF = O_OFF + (O_STAGE ? Q_TILES * TILE_BYTES : 0);
+  static constexpr int BAR_OFF = O_OFF + (O_STAGE ? Q_TILES * O_TILE_BYTES : 0);
   // TMEM columns: S_0 [0,128), S_1 [128,256), O_t at O_COL + D*t; with
   // SEP_P (d = 64) P_t gets its own 64 columns at P_COL + 64*t, otherwise P_t
-  // overwrites the first 64 columns of S_t.
+  // overwrites the first P_WORDS columns of S_t. P is packed 4 / ESZ values
+  // per 32-bit column: 64 columns of bf16 pairs or 32 of e4m3 quads.
   static constexpr bool SEP_P = (D == 64);
+  static constexpr int P_WORDS = BLOCK_N * ESZ / 4;
   static constexpr uint32_t O_COL = 2 * BLOCK_N;
   static constexpr uint32_t P_COL = SEP_P ? O_COL + Q_TILES * D : 0;
-  static constexpr uint32_t P_STRIDE = SEP_P ? BLOCK_N / 2 : BLOCK_N;
-  static_assert(!SEP_P || P_COL + Q_TILES * BLOCK_N / 2 <= 512, "TMEM budget");
+  static constexpr uint32_t P_STRIDE = SEP_P ? P_WORDS : BLOCK_N;
+  static_assert(!SEP_P || P_COL + Q_TILES * P_WORDS <= 512, "TMEM budget");
   static constexpr int NBAR = 6 * Q_TILES + NK + NV + NR + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false);  // Q, K both K-major
-  static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, true);     // V is MN-major
+  static constexpr uint32_t IDESC_S =
+      F8 ? idesc_e4m3_f32(128, 128, false) : idesc_bf16_f32(128, 128, false);  // Q, K both K-major
+  static constexpr uint32_t IDESC_O = F8 ? idesc_e4m3_f32(128, D, true) : idesc_bf16_f32(128, D, true);  // V MN-major
   // Softmax tuning: exponential pairs (of 16 per 32 columns) computed on the
   // FMA pipe instead of the MUFU unit, and the lazy-rescale threshold.
   static constexpr int EMU_PAIRS = (D == 64) ? FA_EMU_PAIRS_D64 : FA_EMU_PAIRS_D128;
@@ -148,9 +161,6 @@ struct PrefillCfg {
   // walks the issue loop: its waits then need no warp vote, and lanes 1-31
   // wait once, at the end, for the drain.
   static constexpr bool SOLO_ISSUE = (D == 64) ? FA_SOLO_ISSUE_D64 : FA_SOLO_ISSUE_D128;
-  // One issuing thread for both Q tiles (separate P columns only): it keeps
-  // each tile's next product in view and issues whichever is ready.
-  static constexpr bool SINGLE_ISSUE = SEP_P && FA_SINGLE_ISSUE_D64;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -167,19 +177,41 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 }
 
 // One query row's scores s[0..127] (fp32 bit patterns, masked ones -inf) ->
-// P = 2^(s * sl2 - m) as 64 bf16 pairs in pk_all, returning the row sum of
-// the fp32 exponentials. EMU pairs of every 16 use the FMA-pipe exponential.
+// P = 2^(s * sl2 - m) as 64 bf16 pairs written over s[0..63] (pair i after
+// scores 2i and 2i + 1 were read, so no score is overwritten before its
+// use), returning the row sum of the fp32 exponentials. EMU pairs of every
+// 16 use the FMA-pipe exponential.
 // With MASKED, -inf scores give exactly 0 on both exponential paths.
 // When poll_bar is nonzero, the barrier at that shared address is polled
 // (parity poll_par) halfway through and the result left in *poll_res.
-template <bool MASKED, int EMU>
-__device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x2, uint64_t nm2, uint32_t* pk_all,
-                                                uint32_t poll_bar, uint32_t poll_par, uint32_t* poll_res) {
+template <bool MASKED, int EMU, bool F8 = false>
+__device__ __forceinline__ float softmax_tile_p(uint32_t* s, uint64_t sl2x2, uint64_t nm2, uint32_t poll_bar,
+                                                uint32_t poll_par, uint32_t* poll_res) {
   uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+  if constexpr (F8) {
+    // e4m3 P: four exponentials per packed word, word w = keys 4w .. 4w + 3
+    // written over s[w] (its scores were read first). ex2(-inf) = 0.
+#pragma unroll
+    for (int w = 0; w < BLOCK_N / 4; ++w) {
+      if (FA_EARLY_POLL && w == BLOCK_N / 8 && poll_bar != 0u) *poll_res = mbar_test(poll_bar, poll_par);
+      const int c = 4 * w;
+      const uint64_t xa = ffma2(f2pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nm2);
+      const uint64_t xb = ffma2(f2pack(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, nm2);
+      float x0, x1, x2, x3;
+      f2unpack(xa, x0, x1);
+      f2unpack(xb, x2, x3);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+      acc2[w & 3] = fadd2(acc2[w & 3], fadd2(f2pack(p0, p1), f2pack(p2, p3)));
+      s[w] = pack_e4m3x4(p0, p1, p2, p3);
+    }
+    float a0, a1, a2, a3;
+    f2unpack(fadd2(acc2[0], acc2[1]), a0, a1);
+    f2unpack(fadd2(acc2[2], acc2[3]), a2, a3);
+    return (a0 + a1) + (a2 + a3);
+  }
 #pragma unroll
   for (int ch = 0; ch < BLOCK_N / 32; ++ch) {
     if (FA_EARLY_POLL && ch == BLOCK_N / 64 && poll_bar != 0u) *poll_res = mbar_test(poll_bar, poll_par);
-    uint32_t* pk = pk_all + ch * 16;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int c = ch * 32 + 2 * i;
@@ -202,7 +234,7 @@ __device__ __forceinline__ float softmax_tile_p(const uint32_t* s, uint64_t sl2x
       acc2[i & 3] = fadd2(acc2[i & 3], p2);
       float p0, p1;
       f2unpack(p2, p0, p1);
-      pk[i] = pack_bf16x2(p0, p1);
+      s[ch * 16 + i] = pack_bf16x2(p0, p1);  // pair index (ch * 32 + 2i) / 2
     }
   }
   float a0, a1, a2, a3;
@@ -275,12 +307,12 @@ __device__ __forceinline__ int unit_of(int c, int k, int G, bool snake) {
   return k * G + ((snake && (k & 1)) ? (G - 1 - c) : c);
 }
 
-template <int D>
-__global__ void __launch_bounds__(PREFILL_THREADS, 1)
+template <int D, bool F8>
+__global__ void __launch_bounds__(prefill_threads(D), 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                       const PrefillParams p) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<D, F8>;
   constexpr int NK = C::NK, NV = C::NV, NR = C::NR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -348,7 +380,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     }
     for (int i = 0; i < NK; ++i) mbar_init(full_k + i, 1);
     for (int i = 0; i < NV; ++i) mbar_init(full_v + i, 1);
-    for (int i = 0; i < NR; ++i) mbar_init(rel + i, C::SINGLE_ISSUE ? 1 : Q_TILES);  // each MMA issuer
+    for (int i = 0; i < NR; ++i) mbar_init(rel + i, Q_TILES);  // both MMA-issuing warps
     mbar_init(unit_done, Q_TILES);
     mbar_init(drain, Q_TILES);
     *abort_flag = 0;
@@ -399,7 +431,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
             uint8_t* dst = sK + (g % NK) * C::TILE_BYTES;
             mbar_arrive_expect_tx(full_k + (g % NK), C::TILE_BYTES);
             for (int b = 0; b < C::NBOX; ++b)
-              tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full_k + (g % NK), 64 * b, jj * BLOCK_N, w.bh);
+              tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full_k + (g % NK), C::BOX_ELEMS * b, jj * BLOCK_N, w.bh);
           }
           ++nlk;
           if (!(ok = wait_rel(g - NV))) break;
@@ -407,7 +439,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
             uint8_t* dst = sV + (g % NV) * C::TILE_BYTES;
             mbar_arrive_expect_tx(full_v + (g % NV), C::TILE_BYTES);
             for (int b = 0; b < C::NBOX; ++b)
-              tma_load_3d(dst + b * C::BOX_BYTES, &tmV, full_v + (g % NV), 64 * b, jj * BLOCK_N, w.bh);
+              tma_load_3d(dst + b * C::BOX_BYTES, &tmV, full_v + (g % NV), C::BOX_ELEMS * b, jj * BLOCK_N, w.bh);
           }
           ++nlv;
         }
@@ -442,7 +474,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
             if (t ? w.act1 : w.act0) {
               mbar_arrive_expect_tx(q_full + t, C::TILE_BYTES);
               for (int b = 0; b < C::NBOX; ++b)
-                tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full + t, 64 * b,
+                tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full + t, C::BOX_ELEMS * b,
                             w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh);
             } else {
               mbar_arrive(q_full + t);  // a tile this unit does not compute: the phase completes empty
@@ -454,161 +486,6 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       if (!ok && leader) {
         for (int t = 0; t < Q_TILES; ++t)
           if (issued[t] > 0) mbar_wait_drain(q_full + t, (issued[t] - 1) & 1, lim);
-      }
-      __syncwarp();
-    } else if (C::SINGLE_ISSUE) {
-      // ------------------------------------------------------ single MMA issuer
-      // Lane 0 of the first MMA warp issues every product of both Q tiles.
-      // tcgen05.mma issue runs only about one instruction ahead of the
-      // tensor pipe, so the issuer never blocks on one tile while the other
-      // has a product ready: it polls both tiles' next products
-      // (non-blocking) and issues the first one whose inputs are ready,
-      // trying the tile it did not serve last first.
-      // Per tile t and unit, with n key tiles, the products come in the
-      // order S_0, S_1, PV_0, S_2, PV_1, ..., PV_{n-1}: S_{j+1} may go as soon
-      // as the softmax has read S_j (s_free), PV_j once P_j is stored (p_full).
-      // Each tile walks the CTA's units on its own; a key tile is released
-      // (rel, one commit) once both tiles have issued every product that
-      // reads it, or have passed the unit that holds it.
-      if (pw == 1 && lane == 0) {
-        constexpr uint32_t DHI = sdesc_sw128_hi(1024);
-        const uint32_t k_lo = sdesc_sw128_lo(smem_u32(sK), 16);
-        const uint32_t v_lo = sdesc_sw128_lo(smem_u32(sV), C::BOX_BYTES);
-        const uint32_t idesc_s = C::IDESC_S | (p.negate_s ? IDESC_NEGATE_A : 0u);
-        struct TileState {
-          int k;        // unit (index in this CTA's sequence)
-          int n, nmax;  // key tiles of this tile / of the unit
-          int g0;       // ring position of the unit's first key tile
-          int c;        // this tile's steps in earlier units (barrier phases)
-          int ns, npv;  // S / PV products issued in this unit
-          bool live;    // the unit exists
-        };
-        TileState ts[Q_TILES];
-        auto enter = [&](TileState& x, int t, int k, int g0, int c) {
-          x.k = k;
-          x.g0 = g0;
-          x.c = c;
-          x.ns = 0;
-          x.npv = 0;
-          const int u = unit_at(k);
-          x.live = u < U;
-          if (x.live) {
-            const Unit w = unit_info(p, u, kv_keep);
-            x.n = t ? w.n1 : w.n0;
-            x.nmax = max(w.n0, w.n1);
-          } else {
-            x.n = x.nmax = 0;
-          }
-        };
-        enter(ts[0], 0, 0, 0, 0);
-        enter(ts[1], 1, 0, 0, 0);
-        bool issued_any = false;
-        bool ok = true;
-        int released = 0;  // key tiles below this ring position are released
-        // ring position below which tile t has issued every product it needs
-        auto done_pos = [&](const TileState& x) { return x.live ? x.g0 + x.npv : INT_MAX; };
-        // Tries to issue tile t's next product; returns true if it did (or
-        // if it moved the tile to its next unit).
-        auto try_tile = [&](int t) -> bool {
-          TileState& x = ts[t];
-          if (!x.live) return false;
-          if (x.ns == x.n && x.npv == x.n) {
-            // unit finished for this tile. A tile without key tiles releases
-            // its Q buffer once its Q load has landed (the Q producer then
-            // loads the next unit's Q into it).
-            if (x.n == 0 && C::O_STAGE) {
-              if (!mbar_test(smem_u32(q_full + t), x.k & 1)) return false;
-              mbar_arrive(q_free + t);
-            }
-            enter(x, t, x.k + 1, x.g0 + x.nmax, x.c + x.n);
-            return true;
-          }
-          if (x.ns < x.n && x.ns <= x.npv + 1) {
-            const int j = x.ns;
-            const int g = x.g0 + j;
-            const int cc = x.c + j;
-            bool rdy = mbar_test(smem_u32(full_k + (g % NK)), (g / NK) & 1);
-            if (rdy && cc > 0) rdy = mbar_test(smem_u32(s_free + t), (cc - 1) & 1);
-            if (rdy && j == 0) rdy = mbar_test(smem_u32(q_full + t), x.k & 1);
-            if (rdy) {
-              tc_fence_after();
-              const uint32_t q_lo = sdesc_sw128_lo(smem_u32(sQ) + t * C::TILE_BYTES, 16);
-              const uint32_t kb = k_lo + static_cast<uint32_t>(((g % NK) * C::TILE_BYTES) >> 4);
-              const uint32_t dS = tmem + BLOCK_N * t;
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-                mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(s_full + t);
-              if (j == x.n - 1 && C::O_STAGE) mma_commit(q_free + t);  // Q_t read by its last S
-              issued_any = true;
-              ++x.ns;
-              return true;
-            }
-          }
-          if (x.npv < x.ns) {
-            const int j = x.npv;
-            const int g = x.g0 + j;
-            const int cc = x.c + j;
-            bool rdy = mbar_test(smem_u32(p_full + t), cc & 1);
-            if (rdy) rdy = mbar_test(smem_u32(full_v + (g % NV)), (g / NV) & 1);
-            if (rdy) {
-              tc_fence_after();
-              const uint32_t vb = v_lo + static_cast<uint32_t>(((g % NV) * C::TILE_BYTES) >> 4);
-              const uint32_t dO = tmem + C::O_COL + D * t;
-              const uint32_t aP = tmem + C::P_COL + C::P_STRIDE * t;
-#pragma unroll
-              for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-                mma_ts_w(dO, aP + kk * 8, vb + kk * (2048 >> 4), DHI, C::IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-              mma_commit(o_done + t);
-              issued_any = true;
-              ++x.npv;
-              return true;
-            }
-          }
-          return false;
-        };
-        int pref = 0;
-        uint64_t idle_t0 = 0;
-        uint32_t idle_n = 0;
-        while (ts[0].live || ts[1].live) {
-          bool moved = try_tile(pref);
-          if (moved) {
-            pref ^= 1;
-          } else {
-            moved = try_tile(pref ^ 1);
-          }
-          // release the key tiles both tiles are done with
-          const int rel_to = min(done_pos(ts[0]), done_pos(ts[1]));
-          for (; released < rel_to && released < INT_MAX; ++released) {
-            if (!ts[0].live && !ts[1].live) break;  // nothing loaded past the last unit
-            if (issued_any) mma_commit(rel + (released % NR));
-            else mbar_arrive(rel + (released % NR));
-          }
-          if (moved) {
-            idle_n = 0;
-            continue;
-          }
-          // nothing ready: bounded idle spell
-          if (idle_n == 0) idle_t0 = globaltimer_ns();
-          if ((++idle_n & 31u) == 0u) {
-            if (*abort_flag) { ok = false; break; }
-            if (globaltimer_ns() - idle_t0 > lim) {
-              *abort_flag = 1;
-              atomicOr(p.status, FA_DEV_TIMEOUT);
-              ok = false;
-              break;
-            }
-          }
-        }
-        (void)ok;
-        if (issued_any) mma_commit(drain);
-        else mbar_arrive(drain);
-        mbar_wait_drain(drain, 0, lim);
-      } else if (lane == 0) {
-        mbar_arrive(drain);
-        mbar_wait_drain(drain, 0, lim);
       }
       __syncwarp();
     } else {
@@ -691,9 +568,10 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           if (lane == 0) {
             const uint32_t kb = k_lo + static_cast<uint32_t>((((g0 + jj) % NK) * C::TILE_BYTES) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < C::KSTEPS_S; ++kk) {
               const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
-              mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
+              if constexpr (F8) mma_ss_w_f8(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
+              else mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
             }
             mma_commit(s_full + t);
             // the unit's last score MMA: Q_t is free once it (and all before it)
@@ -709,8 +587,12 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           if (lane == 0) {
             const uint32_t vb = v_lo + static_cast<uint32_t>((((g0 + jj) % NV) * C::TILE_BYTES) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < BLOCK_N / 16; ++kk)
-              mma_ts_w(dO, aP + kk * 8, vb + kk * (2048 >> 4), DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < C::KSTEPS_PV; ++kk) {
+              // A: 8 TMEM columns (32 bytes of P per row) per K-step; B: PV_KROWS rows of V
+              const uint32_t vk = vb + static_cast<uint32_t>((kk * C::PV_KROWS * 128) >> 4);
+              if constexpr (F8) mma_ts_w_f8(dO, aP + kk * 8, vk, DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+              else mma_ts_w(dO, aP + kk * 8, vk, DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+            }
             mma_commit(o_done + t);
           }
         };
@@ -830,7 +712,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
     const uint64_t sl2x2 = f2pack(sl2, sl2);
     const int delta = p.Nk - p.Nq;
     const int nwords = (p.Nk + 31) >> 5;
-    uint8_t* sO = (C::O_STAGE ? smem + C::O_OFF : sQ) + t * C::TILE_BYTES;
+    uint8_t* sO = C::O_STAGE ? smem + C::O_OFF + t * C::O_TILE_BYTES : sQ + t * C::TILE_BYTES;
     const bool storer = wq == 0 && lane == 0;
     bool ok = true;
     int ct = 0;  // this tile's steps in earlier units
@@ -938,15 +820,14 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
         const float alpha = bump ? ex2_approx(m - m_new) : 1.f;  // 0 while nothing was accumulated
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const uint64_t nm2 = f2pack(-m_use, -m_use);
-        uint32_t pk[BLOCK_N / 2];
         uint32_t o_ready = 0;
         const uint32_t o_poll = (C::SEP_P && j > 0) ? smem_u32(o_done + t) : 0u;
         const uint32_t o_par = ph ^ 1u;  // the previous step's phase
         // (with no FMA-pipe pairs both instantiations are the same code: keep
         // one copy of the unrolled loop in the instruction cache)
         const float rowsum = (C::EMU_PAIRS > 0 && need_mask)
-                                 ? softmax_tile_p<true, C::EMU_PAIRS>(s, sl2x2, nm2, pk, o_poll, o_par, &o_ready)
-                                 : softmax_tile_p<false, C::EMU_PAIRS>(s, sl2x2, nm2, pk, o_poll, o_par, &o_ready);
+                                 ? softmax_tile_p<true, C::EMU_PAIRS, F8>(s, sl2x2, nm2, o_poll, o_par, &o_ready)
+                                 : softmax_tile_p<false, C::EMU_PAIRS, F8>(s, sl2x2, nm2, o_poll, o_par, &o_ready);
         if (C::SEP_P && j > 0) {
           // P_t and O_t are free once PV_{t,j-1} has completed; it ran while
           // the exponentials above were computed. (At a unit's first step the
@@ -958,8 +839,8 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
           }
           tc_fence_after();
         }
-        tmem_st32(tP, pk);
-        tmem_st32(tP + 32, pk + 32);
+        tmem_st32(tP, s);  // P: the packed words now in s[0 .. P_WORDS)
+        if constexpr (C::P_WORDS > 32) tmem_st32(tP + 32, s + 32);
         s_ready = (FA_EARLY_POLL && j + 1 < n) ? mbar_test(smem_u32(s_full + t), ph ^ 1u) : 0u;
         l = fmaf(l, alpha, rowsum);
         // O_t is quiescent here: PV_{t,j-1} has completed (waited above, or before
@@ -1005,7 +886,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       // store has read it (the storer waited for that before this barrier)
       if (C::O_STAGE && k > 0) named_bar_sync(1 + t, 128);
       if (ok && active) {
-        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        const float inv = (l > 0.f) ? p.o_scale / l : 0.f;  // o_scale: the v descale (1 for bf16)
         const uint32_t srow = smem_u32(sO) + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
@@ -1037,7 +918,7 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
       if (storer && *abort_flag == 0) {
         if (active && r0 < p.Nq) {
 #pragma unroll
-          for (int b = 0; b < C::NBOX; ++b) tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
+          for (int b = 0; b < C::NBOX_O; ++b) tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
           bulk_commit_group();
           bulk_wait_group_read_all();
         }
@@ -1056,44 +937,50 @@ __global__ void __launch_bounds__(PREFILL_THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool F8>
 static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
   // Persistent: one CTA per SM walks its share of the units, so the next
   // unit's loads and first MMAs overlap the current one's epilogue. A key
   // mask broadcast over rows (trimmed per unit) gets one CTA per unit, as does
   // a head dimension where that measured faster.
+  using C = PrefillCfg<D, F8>;
   const long long units = p.units;
   const bool trim = p.keep != nullptr && p.msq == 0;
-  const long long ctas =
-      (trim || !PrefillCfg<D>::PERSIST) ? units : std::min<long long>(units, std::max(1, p.max_ctas));
-  fa_prefill_kernel<D><<<static_cast<unsigned>(ctas), PREFILL_THREADS, PrefillCfg<D>::SMEM, stream>>>(tq, tk, tv,
-                                                                                                     to, p);
+  const long long ctas = (trim || !C::PERSIST) ? units : std::min<long long>(units, std::max(1, p.max_ctas));
+  fa_prefill_kernel<D, F8><<<static_cast<unsigned>(ctas), prefill_threads(D), C::SMEM, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
-int prefill_num_regs(int d) {
+// The instantiations: bf16 at d = 64 and 128, e4m3 at d = 128.
+int prefill_num_regs(int d, bool f8) {
   cudaFuncAttributes a{};
-  const cudaError_t e = (d == 64) ? cudaFuncGetAttributes(&a, fa_prefill_kernel<64>)
-                                  : cudaFuncGetAttributes(&a, fa_prefill_kernel<128>);
+  const cudaError_t e = f8        ? cudaFuncGetAttributes(&a, fa_prefill_kernel<128, true>)
+                        : d == 64 ? cudaFuncGetAttributes(&a, fa_prefill_kernel<64, false>)
+                                  : cudaFuncGetAttributes(&a, fa_prefill_kernel<128, false>);
   return e == cudaSuccess ? a.numRegs : -1;
 }
 
-size_t prefill_smem_bytes(int d) {
-  return d == 64 ? PrefillCfg<64>::SMEM : PrefillCfg<128>::SMEM;
+size_t prefill_smem_bytes(int d, bool f8) {
+  return f8 ? PrefillCfg<128, true>::SMEM : d == 64 ? PrefillCfg<64>::SMEM : PrefillCfg<128>::SMEM;
 }
 
-cudaError_t prefill_set_attributes(int d) {
+cudaError_t prefill_set_attributes(int d, bool f8) {
+  if (f8)
+    return cudaFuncSetAttribute(fa_prefill_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                PrefillCfg<128, true>::SMEM);
   if (d == 64)
-    return cudaFuncSetAttribute(fa_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(fa_prefill_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 PrefillCfg<64>::SMEM);
-  return cudaFuncSetAttribute(fa_prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(fa_prefill_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               PrefillCfg<128>::SMEM);
 }
 
-cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_prefill(int d, bool f8, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
-  return d == 64 ? launch_prefill_t<64>(tq, tk, tv, to, p, stream) : launch_prefill_t<128>(tq, tk, tv, to, p, stream);
+  if (f8) return launch_prefill_t<128, true>(tq, tk, tv, to, p, stream);
+  return d == 64 ? launch_prefill_t<64, false>(tq, tk, tv, to, p, stream)
+                 : launch_prefill_t<128, false>(tq, tk, tv, to, p, stream);
 }
 
 }  // namespace fa

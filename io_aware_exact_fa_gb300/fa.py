@@ -37,6 +37,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_E
 EXPORTS = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "fa_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i64, _i64, _i64, _vp]),
+    "fa_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _f, _f, _i, _vp]),
     "fa_fwd_host_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "fa_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
     "fa_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
@@ -126,6 +127,37 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float
                                 B, H, Nq, Nk, d, float(scale), int(bool(causal)),
                                 keep_bits.data_ptr(), int(sb), int(sh), int(sq), st)
         _check(rc, "fa_fwd_masked")
+    return out, lse
+
+
+def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, descale_q: float, descale_k: float,
+            descale_v: float, scale: Optional[float] = None, causal: bool = False,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, with_lse: bool = True,
+            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Forward pass on e4m3 inputs (fa_fwd_fp8): q8 [B,H,Nq,d], k8/v8 [B,H,Nk,d]
+    as uint8 codes (or torch.float8_e4m3fn), each with one descale factor
+    (real value = code value * descale) -> (o bf16, lse fp32)."""
+    q8, k8, v8 = (t.view(torch.uint8) if isinstance(t, torch.Tensor) and t.dtype == torch.float8_e4m3fn else t
+                  for t in (q8, k8, v8))
+    _need(q8, "q8", torch.uint8); _need(k8, "k8", torch.uint8); _need(v8, "v8", torch.uint8)
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    if k8.shape != (B, H, Nk, d) or v8.shape != (B, H, Nk, d):
+        raise ValueError("k8 and v8 must be [B, H, Nk, d] matching q8")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(B, H, Nq, d, dtype=torch.bfloat16, device=q8.device)
+    _need(out, "out")
+    if with_lse and lse is None:
+        lse = torch.empty(B, H, Nq, dtype=torch.float32, device=q8.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32)
+    rc = _lib.fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, float(scale),
+                         float(descale_q), float(descale_k), float(descale_v), int(bool(causal)),
+                         _stream_ptr(stream))
+    _check(rc, "fa_fwd_fp8")
     return out, lse
 
 
