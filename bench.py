@@ -601,10 +601,66 @@ def run_long_context(args, fa, W, flush, stream, warm, world, rank, dev):
         if key == "prefill_8k" and not args.no_backward:
             rec["backward"] = run_backward(args, fa, W, w, [causal], q, k, v, lse, flush, stream, warm, world, rank,
                                            dev)
+        if not w.pad_heads and not args.no_fp8:
+            del q, k, v
+            rec["fp8"] = run_fp8(args, fa, W, w, causal, flush, stream, warm, world, rank, dev)
         out["workloads"][w.name] = rec
-        del q, k, v, o, lse
+        del o, lse
         torch.cuda.empty_cache()
     return out
+
+
+def run_fp8(args, fa, W, w, causal, flush, stream, warm, world, rank, dev):
+    """Time fa_fwd_fp8 on a workload's shape with e4m3 inputs (the same N(0,1)
+    draws quantized per tensor, descale amax / 448), one launch per step, L2
+    flushed between steps outside the events. The roofline peak is the fp8
+    dense rate: the measured bf16 peak times the nominal fp8 / bf16 ratio 2."""
+    import torch
+    (q8, k8, v8), ds = W.make_qkv_fp8(w.B, w.H, w.Nq, w.Nk, w.d, seed=rank, device="cuda")
+    o = torch.empty(w.B, w.H, w.Nq, w.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device=dev)
+
+    def call():
+        fa.fwd_fp8(q8, k8, v8, *ds, scale=w.scale, causal=causal, out=o, lse=lse)
+
+    for _ in range(warm):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError(f"device status not OK after the {w.name} fp8 warm-up")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    n0 = fa.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    launches = fa.launch_count() - n0
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError(f"device status not OK after the {w.name} fp8 timed region")
+    t = max_over_ranks([sum(a.elapsed_time(b) for a, b in ev) / 1e3], world, dev)[0]
+    f = w.flops(causal)
+    ach = K * f / t / 1e12
+    peaks = measured_peaks()
+    peak = 2.0 * peaks["bf16_tflops"]
+    name = w.name + "_fp8"
+    return {"value": whole_job_rate(f, K, t, world) / 1e12, "unit": "TFLOP/s", "ms": t / K * 1e3,
+            "gpu_launches": launches, "dtype": "e4m3 in, bf16 out",
+            "inputs": "the workload's N(0,1) draws quantized per tensor to e4m3 (descale amax / 448)",
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                         "traffic": recorded_traffic("prefill_sm103.cu", name),
+                         "kernel": f"fa_prefill_kernel<{w.d}, e4m3>",
+                         "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8 / bf16 dense ratio)",
+                         "flop_convention": "4*B*H*Nq*Nk*d, halved for causal"},
+            "_window": (t0, t1)}
 
 
 # --------------------------------------------------------------- reference
@@ -659,6 +715,7 @@ def main():
     ap.add_argument("--prefill-h", type=int, default=0, help="override the prefill heads (profiling a small case)")
     ap.add_argument("--dv-b", type=int, default=0, help="override the decode-variant batch (profiling a small case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the e4m3-input legs of the long-context workloads")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the long-context prefill legs (8k and 32k, d=128; reported under 'long_context')")
     ap.add_argument("--e2e-chunk-heads", type=int, default=0,
@@ -781,8 +838,9 @@ def main():
     if lng is not None:
         for rec in lng["workloads"].values():
             rec["clocks"] = sampler.summary(rec.pop("_window"))
-            if "backward" in rec:
-                rec["backward"]["clocks"] = sampler.summary(rec["backward"].pop("_window"))
+            for sub_leg in ("backward", "fp8"):
+                if sub_leg in rec:
+                    rec[sub_leg]["clocks"] = sampler.summary(rec[sub_leg].pop("_window"))
 
     nm = len(modes)
     t_modes = [sum(e[i].elapsed_time(e[i + 1]) for e in ev) / 1e3 for i in range(nm)]
