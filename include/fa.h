@@ -314,6 +314,29 @@ const char* fa_last_error_detail(void);
  * since the process started (for accounting in benchmarks). */
 uint64_t fa_launch_count(void);
 
+/* Debug build (the pages have no counterpart: this checks the implementation).
+ * libfa_gb300_debug.so is the same library compiled with FA_DEBUG=1: its
+ * prefill kernels check, before each access, the coordinates of every TMA
+ * copy (x on a 16-byte boundary and inside the row, the tile starting inside
+ * the tensor, the batch-head index in range), the TMEM lanes and columns of
+ * every tensor-memory load, store and product, and at the end of a launch that
+ * every barrier completed as many phases as its users counted. A failed check
+ * skips the access and records the failure; nothing traps. The release
+ * library compiles the checks out.
+ *   fa_debug_enabled()   1 in the debug build, 0 in the release build.
+ *   fa_debug_record(out) waits for `stream`, copies the current device's
+ *                        8-word record to host `out` and clears it: word 0
+ *                        bits (1 = TMA coordinate, 2 = TMEM range, 4 =
+ *                        barrier phase count), then the first failure's site,
+ *                        block, thread and three values, then the number of
+ *                        failed checks.
+ *   fa_debug_selftest()  launches one warp that runs every check on values it
+ *                        must reject, with no access; afterwards the debug
+ *                        build's record holds bits 1, 2 and 4. */
+int fa_debug_enabled(void);
+fa_status fa_debug_record(uint32_t* out, void* stream);
+fa_status fa_debug_selftest(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

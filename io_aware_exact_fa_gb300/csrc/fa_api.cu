@@ -20,6 +20,7 @@
 #include "decode_grouped.cuh"
 #include "materialized.cuh"
 #include "fa_common.cuh"
+#include "fa_debug.cuh"
 
 #ifndef FA_TAIL_SPLIT
 #define FA_TAIL_SPLIT 1  // split a last, at most half-full round of Q-tile pairs into single tiles
@@ -28,6 +29,8 @@
 namespace fa {
 // One status word per device; kernels atomicOr FA_DEV_* bits into it.
 __device__ unsigned int g_device_status = 0u;
+// The debug build's device check record (fa_debug.cuh); untouched otherwise.
+__device__ unsigned int g_debug_record[FA_DBG_WORDS] = {0u};
 }  // namespace fa
 
 namespace {
@@ -51,6 +54,7 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 struct DeviceState {
   bool ready = false;
   unsigned int* status = nullptr;
+  unsigned int* debug = nullptr;  // the device check record
   int num_sms = 0;
 };
 using fa::kMaxDevices;
@@ -81,6 +85,10 @@ fa_status device_state(DeviceState** out) {
     void* p = nullptr;
     if ((e = cudaGetSymbolAddress(&p, fa::g_device_status)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    void* pd = nullptr;
+    if ((e = cudaGetSymbolAddress(&pd, fa::g_debug_record)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(debug record)");
+    st.debug = static_cast<unsigned int*>(pd);
     st.status = static_cast<unsigned int*>(p);
     if ((e = fa::prefill_set_attributes(64, false)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(d=64)");
     if ((e = fa::prefill_set_attributes(128, false)) != cudaSuccess)
@@ -302,6 +310,7 @@ fa_status prefill_common(const void* q, const void* k, const void* v, void* o, f
   p.scale_log2 = fmaxf(fabsf(scale) * f8.dq * f8.dk * 1.4426950408889634f, 1.17549435e-38f);
   p.negate_s = scale < 0.f ? 1 : 0;
   p.o_scale = f8.dv;
+  p.dbg = FA_DEBUG ? st->debug : nullptr;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = st->status;
   p.max_ctas = st->num_sms;
@@ -783,6 +792,32 @@ fa_status fa_selftest_exp2(const float* x, float* y, int n, void* stream) {
   if (fa_status s = device_state(&st)) return s;
   cudaError_t e = fa::launch_exp2_selftest(x, y, n, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "exp2 self-test launch");
+  t_launches += 1;
+  return FA_OK;
+}
+
+int fa_debug_enabled(void) { return FA_DEBUG ? 1 : 0; }
+
+fa_status fa_debug_record(uint32_t* out, void* stream) {
+  t_detail[0] = 0;
+  if (!out) return fail(FA_ERR_INVALID_ARG, "out must hold 8 words");
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(out, st->debug, fa::FA_DBG_WORDS * sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st->debug, 0, fa::FA_DBG_WORDS * sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "debug record read-back");
+  return FA_OK;
+}
+
+fa_status fa_debug_selftest(void* stream) {
+  t_detail[0] = 0;
+  DeviceState* st = nullptr;
+  if (fa_status s = device_state(&st)) return s;
+  cudaError_t e = fa::launch_debug_selftest(st->debug, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "debug self-test launch");
   t_launches += 1;
   return FA_OK;
 }

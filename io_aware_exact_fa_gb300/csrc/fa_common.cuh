@@ -79,6 +79,7 @@ struct PrefillParams {
   unsigned int* status;      // device status word
   int max_ctas;              // CTAs of a persistent launch (the SM count)
   int units;                 // work units: Q-tile pairs, then single Q tiles (see split_from)
+  unsigned int* dbg;         // debug build: the device check record (FA_DBG_WORDS words); else nullptr
   int split_from;            // units from here on are single tiles of the last pairs
 };
 
@@ -124,5 +125,6 @@ cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
 cudaError_t bwd_set_attributes(int d);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int* status, cudaStream_t stream);
 cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream);
+cudaError_t launch_debug_selftest(unsigned int* rec, cudaStream_t stream);
 
 }  // namespace fa

@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <climits>
 
+#include "fa_debug.cuh"
 #include "fa_ptx.cuh"
 
 namespace fa {
@@ -398,6 +399,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   // Every role walks the same unit sequence; barrier phases run on across
   // units (counts of units, key tiles and per-tile steps done so far).
   auto unit_at = [&](int k) { return unit_of(cta, k, G, snake); };
+  int dbg_count0 = 0, dbg_count1 = 0;  // debug build: steps of a tile (softmax) / K and V loads (producer)
 
   if (producer) {
     setmaxnreg_dec<prefill_producer_regs(D)>();
@@ -431,7 +433,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             uint8_t* dst = sK + (g % NK) * C::TILE_BYTES;
             mbar_arrive_expect_tx(full_k + (g % NK), C::TILE_BYTES);
             for (int b = 0; b < C::NBOX; ++b)
-              tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full_k + (g % NK), C::BOX_ELEMS * b, jj * BLOCK_N, w.bh);
+              if (dbg_tma_ok(p.dbg, DBG_LOAD_K, C::BOX_ELEMS * b, jj * BLOCK_N, w.bh, D, p.Nk, p.B * p.H, C::ESZ))
+                tma_load_3d(dst + b * C::BOX_BYTES, &tmK, full_k + (g % NK), C::BOX_ELEMS * b, jj * BLOCK_N, w.bh);
           }
           ++nlk;
           if (!(ok = wait_rel(g - NV))) break;
@@ -439,7 +442,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             uint8_t* dst = sV + (g % NV) * C::TILE_BYTES;
             mbar_arrive_expect_tx(full_v + (g % NV), C::TILE_BYTES);
             for (int b = 0; b < C::NBOX; ++b)
-              tma_load_3d(dst + b * C::BOX_BYTES, &tmV, full_v + (g % NV), C::BOX_ELEMS * b, jj * BLOCK_N, w.bh);
+              if (dbg_tma_ok(p.dbg, DBG_LOAD_V, C::BOX_ELEMS * b, jj * BLOCK_N, w.bh, D, p.Nk, p.B * p.H, C::ESZ))
+                tma_load_3d(dst + b * C::BOX_BYTES, &tmV, full_v + (g % NV), C::BOX_ELEMS * b, jj * BLOCK_N, w.bh);
           }
           ++nlv;
         }
@@ -449,6 +453,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         for (int n = max(0, nlk - NK); n < nlk; ++n) mbar_wait_drain(full_k + (n % NK), (n / NK) & 1, lim);
         for (int n = max(0, nlv - NV); n < nlv; ++n) mbar_wait_drain(full_v + (n % NV), (n / NV) & 1, lim);
       }
+      dbg_count0 = nlk;
+      dbg_count1 = nlv;
       __syncwarp();
     } else if (pw == 3) {
       // ------------------------------------------------------- Q TMA producer
@@ -473,9 +479,13 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
           if (leader) {
             if (t ? w.act1 : w.act0) {
               mbar_arrive_expect_tx(q_full + t, C::TILE_BYTES);
+              // (the second tile of the last pair may start past Nq: it then
+              // reads zeros and computes nothing; the pair grid bounds it)
               for (int b = 0; b < C::NBOX; ++b)
-                tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full + t, C::BOX_ELEMS * b,
-                            w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh);
+                if (dbg_tma_ok(p.dbg, DBG_LOAD_Q, C::BOX_ELEMS * b, w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh,
+                               D, p.n_qpairs * Q_TILES * BLOCK_M, p.B * p.H, C::ESZ))
+                  tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full + t, C::BOX_ELEMS * b,
+                              w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh);
             } else {
               mbar_arrive(q_full + t);  // a tile this unit does not compute: the phase completes empty
             }
@@ -570,6 +580,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
 #pragma unroll
             for (int kk = 0; kk < C::KSTEPS_S; ++kk) {
               const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
+              if (!dbg_tmem_mma_ok(p.dbg, DBG_MMA_S, dS, BLOCK_N, 0u, 0)) continue;
               if constexpr (F8) mma_ss_w_f8(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
               else mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
             }
@@ -590,6 +601,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             for (int kk = 0; kk < C::KSTEPS_PV; ++kk) {
               // A: 8 TMEM columns (32 bytes of P per row) per K-step; B: PV_KROWS rows of V
               const uint32_t vk = vb + static_cast<uint32_t>((kk * C::PV_KROWS * 128) >> 4);
+              if (!dbg_tmem_mma_ok(p.dbg, DBG_MMA_PV, dO, D, aP + kk * 8, 8)) continue;
               if constexpr (F8) mma_ts_w_f8(dO, aP + kk * 8, vk, DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
               else mma_ts_w(dO, aP + kk * 8, vk, DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
             }
@@ -753,10 +765,14 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         }
         tc_fence_after();
         uint32_t s[BLOCK_N];
-        tmem_ld32(tS + 0, s);
-        tmem_ld32(tS + 32, s + 32);
-        tmem_ld32(tS + 64, s + 64);
-        tmem_ld32(tS + 96, s + 96);
+        if (FA_DEBUG && !dbg_tmem_warp_ok(p.dbg, DBG_LD_S, tS, BLOCK_N)) {
+          for (int c = 0; c < BLOCK_N; ++c) s[c] = 0u;  // the load is skipped
+        } else {
+          tmem_ld32(tS + 0, s);
+          tmem_ld32(tS + 32, s + 32);
+          tmem_ld32(tS + 64, s + 64);
+          tmem_ld32(tS + 96, s + 96);
+        }
         tmem_ld_wait32(s);
         reg_fence32(s + 32);
         reg_fence32(s + 64);
@@ -839,8 +855,10 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
           }
           tc_fence_after();
         }
-        tmem_st32(tP, s);  // P: the packed words now in s[0 .. P_WORDS)
-        if constexpr (C::P_WORDS > 32) tmem_st32(tP + 32, s + 32);
+        if (dbg_tmem_warp_ok(p.dbg, DBG_ST_P, tP, C::P_WORDS)) {
+          tmem_st32(tP, s);  // P: the packed words now in s[0 .. P_WORDS)
+          if constexpr (C::P_WORDS > 32) tmem_st32(tP + 32, s + 32);
+        }
         s_ready = (FA_EARLY_POLL && j + 1 < n) ? mbar_test(smem_u32(s_full + t), ph ^ 1u) : 0u;
         l = fmaf(l, alpha, rowsum);
         // O_t is quiescent here: PV_{t,j-1} has completed (waited above, or before
@@ -849,6 +867,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
           const uint64_t al2 = f2pack(alpha, alpha);
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
+            if (!dbg_tmem_warp_ok(p.dbg, DBG_ST_O, tO + ch * 32, 32)) continue;
             uint32_t o[32];
             tmem_ld32(tO + ch * 32, o);
             tmem_ld_wait32(o);
@@ -891,7 +910,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
-          if (n > 0) {
+          if (n > 0 && dbg_tmem_warp_ok(p.dbg, DBG_LD_O, tO + ch * 32, 32)) {
             tmem_ld32(tO + ch * 32, o);
             tmem_ld_wait32(o);
           } else {
@@ -918,7 +937,9 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       if (storer && *abort_flag == 0) {
         if (active && r0 < p.Nq) {
 #pragma unroll
-          for (int b = 0; b < C::NBOX_O; ++b) tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
+          for (int b = 0; b < C::NBOX_O; ++b)
+            if (dbg_tma_ok(p.dbg, DBG_STORE_O, 64 * b, r0, bh, D, p.Nq, p.B * p.H, 2))
+              tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
           bulk_commit_group();
           bulk_wait_group_read_all();
         }
@@ -927,14 +948,52 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       ct += n;
     }
     if (storer) bulk_wait_group_all();  // the last stores are complete before the CTA exits
+    dbg_count0 = ct;
   }
 
   tc_fence_before();
   __syncthreads();
+  if (FA_DEBUG && *abort_flag == 0 && lane == 0) {
+    // every barrier has completed as many phases as its users counted
+    if (!producer && (sw & 3) == 0) {
+      const int t = sw >> 2;
+      dbg_phase_check(p.dbg, DBG_PHASE_S, smem_u32(s_full + t), dbg_count0, t);
+      dbg_phase_check(p.dbg, DBG_PHASE_P, smem_u32(p_full + t), dbg_count0, t);
+      dbg_phase_check(p.dbg, DBG_PHASE_O, smem_u32(o_done + t), dbg_count0, t);
+      if (C::SEP_P) dbg_phase_check(p.dbg, DBG_PHASE_SFREE, smem_u32(s_free + t), dbg_count0, t);
+    } else if (producer && pw == 0) {
+      for (int i = 0; i < NK; ++i)
+        dbg_phase_check(p.dbg, DBG_PHASE_K, smem_u32(full_k + i), dbg_count0 > i ? (dbg_count0 - i + NK - 1) / NK : 0, i);
+      for (int i = 0; i < NV; ++i)
+        dbg_phase_check(p.dbg, DBG_PHASE_V, smem_u32(full_v + i), dbg_count1 > i ? (dbg_count1 - i + NV - 1) / NV : 0, i);
+    }
+  }
   if (alloc_warp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+// Runs every debug check once on values it must reject (a misaligned TMA x
+// coordinate, another warp's TMEM lanes, columns past the allocation, a
+// barrier whose phase count disagrees), performing no access at all. In a
+// debug build each check must set its bit; in a release build the checks are
+// compiled out and the record stays clear.
+__global__ void fa_debug_selftest_kernel(unsigned int* rec) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;  // lane 0 of warp 0: TMEM lane quarter 0
+  (void)dbg_tma_ok(rec, DBG_SELFTEST, 8, 0, 0, 64, 128, 1, 1);           // x = 8 one-byte codes: off 16 bytes
+  (void)dbg_tmem_warp_ok(rec, DBG_SELFTEST, 32u << 16, 32);              // lanes 32..63 from warp 0
+  (void)dbg_tmem_mma_ok(rec, DBG_SELFTEST, 480u, 64, 0u, 0);             // columns 480..543
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_arrive(&bar);                                                     // one phase completed ...
+  dbg_phase_check(rec, DBG_SELFTEST, smem_u32(&bar), 2, 0);              // ... where two were counted
+}
+
+cudaError_t launch_debug_selftest(unsigned int* rec, cudaStream_t stream) {
+  fa_debug_selftest_kernel<<<1, 32, 0, stream>>>(rec);
+  return cudaGetLastError();
 }
 
 template <int D, bool F8>

@@ -57,11 +57,29 @@ EXPORTS = {
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_last_error_detail": (ctypes.c_char_p, []),
     "fa_launch_count": (_u64, []),
+    "fa_debug_enabled": (_i, []),
+    "fa_debug_record": (_i, [_vp, _vp]),
+    "fa_debug_selftest": (_i, [_vp]),
 }
 for _name, (_res, _args) in EXPORTS.items():
     _fn = getattr(_lib, _name)
     _fn.restype = _res
     _fn.argtypes = _args
+
+
+def debug_library() -> ctypes.CDLL:
+    """The device-checking build (libfa_gb300_debug.so, FA_DEBUG=1; see
+    include/fa.h), with the same entry points as the release library. Build it
+    with ``build.build(debug=True)``."""
+    path = os.path.join(_HERE, "libfa_gb300_debug.so")
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m io_aware_exact_fa_gb300.build --debug`")
+    dl = ctypes.CDLL(path)
+    for name, (res, args) in EXPORTS.items():
+        fn = getattr(dl, name)
+        fn.restype = res
+        fn.argtypes = args
+    return dl
 
 
 class FAError(RuntimeError):
