@@ -37,6 +37,10 @@
 
 namespace fa {
 
+#ifndef FA_BWD_ELECT_ISSUE
+#define FA_BWD_ELECT_ISSUE 1
+#endif
+
 namespace {
 
 constexpr int BWD_THREADS = 512;
@@ -58,10 +62,13 @@ struct BwdCfg {
   // products; at d = 128 neither fits.
   static constexpr bool SEP = (D == 64);
   static constexpr int NDS = SEP ? 2 : 1;
-  // At d = 64 (where it measured faster) only lane 0 of the MMA warp walks
-  // the issue loop: its waits need no warp vote, and lanes 1-31 wait once, at
-  // the end, for the drain.
-  static constexpr bool SOLO_ISSUE = (D == 64);
+  // The MMA warp walks the issue loop converged, and the lane elect.sync
+  // picks issues every MMA and commit: one thread then keeps the tensor pipe
+  // fed with the N = 64 products, which a loop run by lane 0 alone issues at
+  // about half the pipe's rate. (Otherwise, at d = 64, lane 0 walks the loop
+  // alone: its waits need no warp vote.)
+  static constexpr bool ELECT_ISSUE = FA_BWD_ELECT_ISSUE;
+  static constexpr bool SOLO_ISSUE = !ELECT_ISSUE && (D == 64);
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;                 // 2 stages of (Q, dO)
@@ -367,6 +374,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // S^T and dP^T first, then dV_i, dQ_i and dK_i, so the next softmax-grad
     // overlaps all three.
     const bool leader = lane == 0;
+    // the thread that issues the MMAs and commits
+    auto issuer = [&]() -> bool {
+      if constexpr (C::ELECT_ISSUE) return elect_one();
+      else return leader;
+    };
     bool ok = true;
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
       ok = mbar_wait(bar, parity, lim, p.status, abort_flag);
@@ -389,19 +401,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     auto issue_s_dp = [&](int it) {
       const uint32_t qb = stage(it);
       const uint32_t q_lo = sdesc_sw128_lo(qb, 16), do_lo = sdesc_sw128_lo(qb + C::TILE_BYTES, 16);
-      if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_w(tST, k_lo + kmaj(kk), DHI, q_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (issuer()) mma_ss_w(tST, k_lo + kmaj(kk), DHI, q_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
       // at d = 128, dP^T (the dP^T columns) only after the previous dQ_i was read out
       if (!C::SEP && it > 0 && !wait_bar(dq_free, (it - 1) & 1)) return false;
-      if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_w(tDPT, v_lo + kmaj(kk), DHI, do_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
-        mma_commit(s_full);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (issuer()) mma_ss_w(tDPT, v_lo + kmaj(kk), DHI, do_lo + kmaj(kk), DHI, C::IDESC_T, kk > 0 ? 1u : 0u);
+      if (issuer()) mma_commit(s_full);
       return true;
     };
     const bool walks = !C::SOLO_ISSUE || leader;  // this lane runs the issue loop
@@ -416,25 +424,30 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       auto issue_dq = [&]() {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss_w(tDQ, dsmn_lo + mnmaj(kk), DHI, kmn_lo + mnmaj(kk), DHI, C::IDESC_AB_MN, kk > 0 ? 1u : 0u);
-        mma_commit(dq_full);
+          if (issuer())
+            mma_ss_w(tDQ, dsmn_lo + mnmaj(kk), DHI, kmn_lo + mnmaj(kk), DHI, C::IDESC_AB_MN, kk > 0 ? 1u : 0u);
+        if (issuer()) mma_commit(dq_full);
       };
       // dV += P^T dO_i (A = P^T from TMEM: queries 16 kk.. of half kk / 4 at
       // tPT + PT_HALF (kk / 4) + 8 (kk % 4); B = dO_i MN-major)
       auto issue_dv = [&]() {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts_w(tDV, tPT + (kk >> 2) * C::PT_HALF + (kk & 3) * 8, domn_lo + mnmaj(kk), DHI, C::IDESC_B_MN,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(dv_done);
+          if (issuer())
+            mma_ts_w(tDV, tPT + (kk >> 2) * C::PT_HALF + (kk & 3) * 8, domn_lo + mnmaj(kk), DHI, C::IDESC_B_MN,
+                     (it > 0 || kk > 0) ? 1u : 0u);
+        if (issuer()) mma_commit(dv_done);
       };
       // dK += dS^T Q_i (A = dS^T K-major, B = Q_i MN-major)
       auto issue_dk = [&]() {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss_w(tDK, ds_lo + kmaj(kk), DHI, qmn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(step_done);
-        mma_commit(q_empty + (it & 1));
+          if (issuer())
+            mma_ss_w(tDK, ds_lo + kmaj(kk), DHI, qmn_lo + mnmaj(kk), DHI, C::IDESC_B_MN, (it > 0 || kk > 0) ? 1u : 0u);
+        if (issuer()) {
+          mma_commit(step_done);
+          mma_commit(q_empty + (it & 1));
+        }
       };
       if (!wait_bar(p_full, it & 1)) break;
       if constexpr (C::SEP) {
@@ -443,32 +456,30 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           if (!wait_bar(q_full + ((it + 1) & 1), ((it + 1) >> 1) & 1)) break;
           if (!issue_s_dp(it + 1)) break;
         }
-        if (leader) issue_dv();
+        issue_dv();
         // dQ_i into the dQ columns once the drain has read dQ_{i-1}
         if (it > 0 && !wait_bar(dq_free, (it - 1) & 1)) break;
-        if (leader) {
-          issue_dq();
-          issue_dk();
-        }
+        issue_dq();
+        issue_dk();
       } else {
-        if (leader) {
-          issue_dq();  // into the dP^T columns, so its drain overlaps dV and dK
-          issue_dv();
-        }
+        issue_dq();  // into the dP^T columns, so its drain overlaps dV and dK
+        issue_dv();
         if (it + 1 < n_it) {
           // the next S^T overwrites P^T_i: only after dV_i read it
           if (!wait_bar(q_full + ((it + 1) & 1), ((it + 1) >> 1) & 1)) break;
           if (!wait_bar(dv_done, it & 1)) break;
           if (!issue_s_dp(it + 1)) break;
         }
-        if (leader) issue_dk();
+        issue_dk();
       }
     }
-    if (leader) {
-      if (n_it > 0) mma_commit(acc_done);
-      else mbar_arrive(acc_done);
-      mbar_drain(acc_done, 0, lim);  // every MMA completed before TMEM is released
+    if (!C::SOLO_ISSUE) __syncwarp();
+    if (n_it > 0) {
+      if (issuer()) mma_commit(acc_done);
+    } else if (leader) {
+      mbar_arrive(acc_done);
     }
+    if (leader) mbar_drain(acc_done, 0, lim);  // every MMA completed before TMEM is released
     __syncwarp();
   } else if (warp >= BWD_SG_WARP0 && warp < BWD_DQ_WARP0) {
     // ---------------------------------------------------------- softmax-grad

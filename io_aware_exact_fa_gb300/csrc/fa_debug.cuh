@@ -24,7 +24,7 @@ constexpr int FA_DBG_WORDS = 8;
 // Sites (word 1 of the record): which access failed.
 enum DbgSite : int {
   DBG_LOAD_Q = 1, DBG_LOAD_K, DBG_LOAD_V, DBG_STORE_O, DBG_MMA_S, DBG_MMA_PV, DBG_LD_S, DBG_ST_P, DBG_LD_O,
-  DBG_ST_O, DBG_PHASE_S, DBG_PHASE_P, DBG_PHASE_O, DBG_PHASE_SFREE, DBG_PHASE_K, DBG_PHASE_V, DBG_SELFTEST = 99
+  DBG_ST_O, DBG_PHASE_S, DBG_PHASE_P, DBG_PHASE_O, DBG_PHASE_SFREE, DBG_PHASE_K, DBG_PHASE_V, DBG_ELECT, DBG_SELFTEST = 99
 };
 
 __device__ __forceinline__ void dbg_fail(unsigned int* rec, unsigned int bit, int site, int v0, int v1, int v2) {

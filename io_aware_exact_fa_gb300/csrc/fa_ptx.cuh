@@ -268,6 +268,27 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 // Arrive once on `bar` when every MMA issued so far by this thread completed.
+// One lane of a converged warp (elect.sync over all 32 lanes; the same lane
+// every time the full warp executes it): the issuing thread of tcgen05 work.
+// Issuing each MMA under this predicate, with the operands computed by the
+// whole warp, lets one thread keep the tensor pipe fed; an MMA loop run by
+// lane 0 alone, or under `lane == 0`, issues about half as fast.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 x;\n\t"
+      "elect.sync x|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r));
+  return r != 0u;
+}
+// The lane elect_one() picks in a converged warp (checked by the debug build).
+__device__ __forceinline__ uint32_t elected_lane() {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync %0|p, 0xffffffff;\n\t}" : "=r"(r));
+  return r;
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
