@@ -25,6 +25,9 @@ struct DecodeGroupedParams {
 cudaError_t launch_decode_grouped(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const DecodeGroupedParams& p, cudaStream_t stream);
 cudaError_t decode_grouped_set_attributes(int d);
+// Rows of the Q tensor map's box the kernel chosen for (d, R = G * Nq query
+// rows per K/V head) loads: the launcher picks the kernel by the same rule.
+int decode_grouped_q_box_rows(int d, int R);
 // The split-KV decode's merge pass alone (defined with the split-KV decode).
 cudaError_t launch_decode_merge(int d, const DecodeParams& p, cudaStream_t stream);
 

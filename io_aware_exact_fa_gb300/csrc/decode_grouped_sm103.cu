@@ -354,6 +354,444 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Keys on the TMEM lanes (d = 128, at most 16 query rows per K/V head).
+//
+// With G * Nq <= 16 real rows, the 128-row query tile above is mostly padding:
+// it pins 32 KB of Q, two 128-column S buffers and a 128-row O accumulator, so
+// one CTA fills an SM and its set-up is never overlapped. Here the products
+// run transposed, S^T = K Q^T (M = 128 keys, N = 16 rows) and
+// O^T += V^T P^T (M = d, N = 16 rows): TMEM holds two 16-column S^T buffers
+// and a 16-column O^T, P^T goes to shared memory, and with one K and one V
+// stage a CTA needs 74 KB of shared memory: three CTAs share an SM, and one
+// streams while another sets up. (Measured on the GQA decode workloads: three
+// CTAs with one stage each 6.45 / 6.18 TB/s, two with two V stages or two P^T
+// buffers 6.29-6.44 / 5.96-6.13, one with three stages 4.77 / 4.48, the
+// 128-row kernel above 6.02 / 5.78.) The softmax runs one thread per key:
+// the row max and sum over the 128 keys of a tile are warp reductions plus a
+// four-warp exchange.
+//
+// fa_decode_grouped_kt_kernel<NK, NV, NPB, MINB>: one CTA per (split, b, kv
+// head), 192 threads, registers sized for MINB CTAs per SM.
+//   warp 0     TMA producer: Q (16 rows) once, K tiles into a ring of NK
+//              stages, V tiles into a ring of NV stages.
+//   warp 1     TMEM allocator and MMA issuer (converged warp, elected lane):
+//              S^T_j into one of two buffers, the next one issued before PV_j.
+//   warps 2-5  softmax, one key per thread (TMEM lane = key); P^T_j (bf16)
+//              into one of NPB shared buffers in the 128-byte-swizzled
+//              K-major layout the PV product reads.
+namespace {
+
+constexpr int DGT_NP = 16;        // query rows per tile (MMA N)
+constexpr int DGT_D = 128;
+constexpr uint32_t DGT_BAR_ID = 1;  // named barrier of the four softmax warps
+
+constexpr int DGT_THREADS = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int DGT_SM_WARP0 = 2;
+
+template <int NK, int NV, int NPB>
+struct DgtCfg {
+  static constexpr int NP = DGT_NP;
+  static constexpr int TILE = 128 * DGT_D * 2;  // one K or V tile: 128 keys x 128 bf16
+  static constexpr int BOX = 128 * 128;         // one TMA box of a K/V tile: 128 rows x 64 bf16
+  static constexpr int QBOX = NP * 128;         // one box of Q or P^T: NP rows x 64 bf16
+  static constexpr int Q_OFF = 0;               // Q: 2 boxes (d 0-63, 64-127)
+  static constexpr int P_OFF = Q_OFF + 2 * QBOX;  // P^T buffer b (of NPB): 2 boxes (keys 0-63, 64-127)
+  static constexpr int K_OFF = P_OFF + NPB * 2 * QBOX;
+  static constexpr int V_OFF = K_OFF + NK * TILE;
+  static constexpr int RED_OFF = V_OFF + NV * TILE;  // float [2][NP][4] row maxima per warp, [NP][4] row sums
+  static constexpr int BAR_OFF = RED_OFF + 3 * NP * 4 * 4;
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 2 + NPB + 1 + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
+  static_assert(QBOX % 1024 == 0 && K_OFF % 1024 == 0 && V_OFF % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+  static constexpr uint32_t S_COL = 0;        // S^T_0 [0, NP), S^T_1 [NP, 2 NP)
+  static constexpr uint32_t O_COL = 2 * NP;   // O^T [2 NP, 3 NP)
+  static constexpr uint32_t TMEM_COLS = 64;
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, NP, false);          // K and Q K-major
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, NP, false, true);   // A = V^T MN-major, B = P^T K-major
+};
+
+// 16 consecutive 32-bit TMEM columns of the thread's lane.
+__device__ __forceinline__ void tmem_ld16_dg(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait16_dg(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])::"memory");
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+// Named barrier over `count` threads that also returns the AND of `v` over them.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0u;
+}
+// Reduction of 16 values per lane over the 32 lanes of a warp, by halving: at
+// each step a lane keeps half of its values and takes the other half from its
+// partner. On return v[0] of lane l holds the result for value index
+// (l >> 1) & 15. MAX: maximum, else sum.
+template <bool MAX>
+__device__ __forceinline__ void warp_reduce16(float* v, int lane) {
+  auto op = [](float a, float b) { return MAX ? fmaxf(a, b) : a + b; };
+#pragma unroll
+  for (int half = 8, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+    const bool hi = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = hi ? v[i] : v[i + half];
+      const float keep = hi ? v[i + half] : v[i];
+      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, bit));
+    }
+  }
+  v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+}
+
+}  // namespace
+
+template <int NK, int NV, int NPB, int MINB>
+__global__ void __launch_bounds__(DGT_THREADS, MINB)
+    fa_decode_grouped_kt_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                                const __grid_constant__ CUtensorMap tmV, const DecodeGroupedParams p) {
+  using C = DgtCfg<NK, NV, NPB>;
+  constexpr int NP = C::NP;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* q_full = bars;                 // Q landed
+  uint64_t* k_full = q_full + 1;           // [NK] K tile landed
+  uint64_t* k_empty = k_full + NK;         // [NK] S^T of that tile completed
+  uint64_t* v_full = k_empty + NK;         // [NV] V tile landed
+  uint64_t* v_empty = v_full + NV;         // [NV] PV of that tile completed
+  uint64_t* s_full = v_empty + NV;         // [2] S^T_j computed (buffer j & 1)
+  uint64_t* s_free = s_full + 2;           // [2] S^T_j read by the softmax
+  uint64_t* p_full = s_free + 2;           // [2] P^T_j stored (all 128 softmax threads)
+  uint64_t* pv_done = p_full + 2;          // [NPB] PV_j completed (P^T buffer j % NPB, phase j / NPB)
+  uint64_t* o_last = pv_done + NPB;        // the last PV completed
+  uint64_t* drain = o_last + 1;            // every MMA completed (end of the issuer)
+  float* red = reinterpret_cast<float*>(smem + C::RED_OFF);  // [2][NP][4] maxima, then [NP][4] sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t lim = p.wait_limit_ns;
+  const int s = static_cast<int>(blockIdx.x) % p.S;
+  const int bg = static_cast<int>(blockIdx.x) / p.S;  // b * Hkv + g
+  const int b = bg / p.Hkv;
+  const int L = p.seqlens ? min(max(p.seqlens[b], 0), p.Nk) : p.Nk;
+  const int k0 = s * p.chunk;
+  const int k1 = min(L, k0 + p.chunk);
+  const int n = k1 > k0 ? (k1 - k0 + 127) / 128 : 0;  // key tiles of this split
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(v_full + i, 1);
+      mbar_init(v_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(s_free + i, 128);
+      mbar_init(p_full + i, 128);
+    }
+    for (int i = 0; i < NPB; ++i) mbar_init(pv_done + i, 1);
+    mbar_init(o_last, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == DG_MMA_WARP) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == DG_TMA_WARP) {
+    // ---------------------------------------------------------- TMA producer
+    // K_j goes to slot j % NK once S^T_{j-NK} (its last reader) completed; V_j
+    // to slot j % NV once PV_{j-NV} completed.
+    const bool leader = lane == 0;
+    bool ok = true;
+    int nk = 0, nv = 0;
+    if (leader && n > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, 2 * C::QBOX);
+      for (int bx = 0; bx < 2; ++bx) tma_load_3d(smem + C::Q_OFF + bx * C::QBOX, &tmQ, q_full, 64 * bx, 0, bg);
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      const int kt0 = k0 + j * 128;
+      if (j >= NK) {
+        ok = __all_sync(0xffffffffu, mbar_wait(k_empty + j % NK, ((j / NK) - 1) & 1, lim, p.status, abort_flag));
+        if (!ok) break;
+      }
+      if (leader) {
+        uint8_t* dst = smem + C::K_OFF + (j % NK) * C::TILE;
+        mbar_arrive_expect_tx(k_full + j % NK, C::TILE);
+        for (int bx = 0; bx < 2; ++bx) tma_load_3d(dst + bx * C::BOX, &tmK, k_full + j % NK, 64 * bx, kt0, bg);
+      }
+      ++nk;
+      if (j >= NV) {
+        ok = __all_sync(0xffffffffu, mbar_wait(v_empty + j % NV, ((j / NV) - 1) & 1, lim, p.status, abort_flag));
+        if (!ok) break;
+      }
+      if (leader) {
+        uint8_t* dst = smem + C::V_OFF + (j % NV) * C::TILE;
+        mbar_arrive_expect_tx(v_full + j % NV, C::TILE);
+        for (int bx = 0; bx < 2; ++bx) tma_load_3d(dst + bx * C::BOX, &tmV, v_full + j % NV, 64 * bx, kt0, bg);
+      }
+      ++nv;
+    }
+    if (leader && n > 0) {
+      // every copy issued lands before the CTA exits
+      mbar_drain(q_full, 0, lim);
+      for (int j = max(0, nk - NK); j < nk; ++j) mbar_drain(k_full + j % NK, (j / NK) & 1, lim);
+      for (int j = max(0, nv - NV); j < nv; ++j) mbar_drain(v_full + j % NV, (j / NV) & 1, lim);
+    }
+    __syncwarp();
+  } else if (warp == DG_MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    // The converged warp walks the loop; the elected lane issues every MMA and
+    // commit.
+    bool ok = true;
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, lim, p.status, abort_flag));
+      tc_fence_after();
+      return ok;
+    };
+    constexpr uint32_t DHI = sdesc_sw128_hi(1024);
+    const uint32_t q_lo = sdesc_sw128_lo(smem_u32(smem + C::Q_OFF), 16);
+    const uint32_t idesc_s = C::IDESC_S | (p.negate_s ? IDESC_NEGATE_A : 0u);
+    // K-major K-step kk (16 elements = 32 bytes): (kk / 4) boxes plus (kk % 4) x 32 bytes in;
+    // MN-major K-step kk (16 keys of V): 16 rows = 2048 bytes in (the two 64-column boxes BOX apart)
+    auto kmaj = [](int kk, int box) { return static_cast<uint32_t>(((kk >> 2) * box + (kk & 3) * 32) >> 4); };
+    auto issue_s = [&](int j) {  // S^T_j = K_j Q^T into buffer j & 1
+      const uint32_t k_lo = sdesc_sw128_lo(smem_u32(smem + C::K_OFF + (j % NK) * C::TILE), 16);
+      const uint32_t tS = tmem + C::S_COL + (j & 1) * NP;
+#pragma unroll
+      for (int kk = 0; kk < DGT_D / 16; ++kk)
+        if (elect_one())
+          mma_ss_w(tS, k_lo + kmaj(kk, C::BOX), DHI, q_lo + kmaj(kk, C::QBOX), DHI, idesc_s, kk > 0 ? 1u : 0u);
+      if (elect_one()) {
+        mma_commit(s_full + (j & 1));
+        mma_commit(k_empty + j % NK);
+      }
+    };
+    auto issue_pv = [&](int j) {  // O^T += V_j^T P^T_j
+      const uint32_t v_lo = sdesc_sw128_lo(smem_u32(smem + C::V_OFF + (j % NV) * C::TILE), C::BOX);
+      const uint32_t p_lo = sdesc_sw128_lo(smem_u32(smem + C::P_OFF + (j % NPB) * 2 * C::QBOX), 16);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        if (elect_one())
+          mma_ss_w(tmem + C::O_COL, v_lo + static_cast<uint32_t>((kk * 2048) >> 4), DHI, p_lo + kmaj(kk, C::QBOX), DHI,
+                   C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+      if (elect_one()) {
+        mma_commit(pv_done + j % NPB);
+        mma_commit(v_empty + j % NV);
+        if (j == n - 1) mma_commit(o_last);
+      }
+    };
+    bool issued_any = false;
+    if (n > 0 && wait_bar(q_full, 0) && wait_bar(k_full, 0)) {
+      issue_s(0);
+      issued_any = true;
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      if (j + 1 < n) {
+        // S^T_{j+1} goes to the buffer the softmax read S^T_{j-1} from
+        if (!wait_bar(k_full + (j + 1) % NK, ((j + 1) / NK) & 1)) break;
+        if (j >= 1 && !wait_bar(s_free + ((j + 1) & 1), ((j - 1) >> 1) & 1)) break;
+        issue_s(j + 1);
+      }
+      if (!wait_bar(p_full + (j & 1), (j >> 1) & 1)) break;
+      if (!wait_bar(v_full + j % NV, (j / NV) & 1)) break;
+      issue_pv(j);
+    }
+    __syncwarp();
+    // every MMA completed before TMEM is released (a commit tracks the elected
+    // lane's MMAs; with none issued a plain arrive completes the phase)
+    if (issued_any) {
+      if (elect_one()) mma_commit(drain);
+    } else if (lane == 0) {
+      mbar_arrive(drain);
+    }
+    mbar_drain(drain, 0, lim);
+    __syncwarp();
+  } else if (warp >= DGT_SM_WARP0 && warp < DGT_SM_WARP0 + 4) {
+    // --------------------------------------------------------------- softmax
+    // Thread = key kr of the tile (its TMEM lane); its NP values are the
+    // scores of the NP query rows (row r: head r / Nq of the group, token
+    // r % Nq, which sees keys below L - Nq + r % Nq + 1; rows past R see none).
+    // The four warps stop together: every exit decision passes a barrier
+    // that ANDs the warps' states, so none waits at a barrier another left.
+    const int wq = warp & 3;  // the TMEM lane quarter this warp may access
+    const int kr = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const int vis_all = max(0, L - p.Nq + 1);  // keys below this are visible to every row of the group
+    float m_ref[NP];  // per row: reference max of P and O (log2 units), moved lazily
+    float lp[NP];     // per row: this thread's part of the row sum on the reference m_ref
+#pragma unroll
+    for (int r = 0; r < NP; ++r) {
+      m_ref[r] = -INFINITY;
+      lp[r] = 0.f;
+    }
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int key = k0 + j * 128 + kr;
+      float x[NP];
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(s_full + (j & 1), (j >> 1) & 1, lim, p.status, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        uint32_t sv[NP];
+        tmem_ld16_dg(tmem + lane_base + C::S_COL + (j & 1) * NP, sv);
+        tmem_ld_wait16_dg(sv);
+        tc_fence_before();
+        mbar_arrive(s_free + (j & 1));
+        const bool all_rows = key < vis_all;
+#pragma unroll
+        for (int r = 0; r < NP; ++r) {
+          const bool vis = r < p.R && (all_rows || key < L - p.Nq + (r % p.Nq) + 1);
+          x[r] = vis ? __uint_as_float(sv[r]) : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < NP; ++r) x[r] = -INFINITY;
+      }
+      // row maxima of the tile: warp reduction, then the four warps' values
+      float v[NP];
+#pragma unroll
+      for (int r = 0; r < NP; ++r) v[r] = x[r];
+      warp_reduce16<true>(v, lane);
+      float* rm = red + (j & 1) * NP * 4;
+      if ((lane & 1) == 0) rm[((lane >> 1) & 15) * 4 + wq] = v[0];
+      ok = bar_and(DGT_BAR_ID, 128, ok);
+      if (!ok) break;
+      float alpha[NP];
+      bool rescale = false;
+#pragma unroll
+      for (int r = 0; r < NP; ++r) {
+        const float4 m4 = reinterpret_cast<const float4*>(rm)[r];
+        const float mx2 = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)) * sl2;  // -inf stays -inf (sl2 > 0)
+        alpha[r] = 1.f;
+        if (mx2 > m_ref[r] + DG_RESCALE_THRESHOLD) {
+          if (m_ref[r] != -INFINITY) {
+            alpha[r] = ex2_approx(m_ref[r] - mx2);
+            rescale = true;
+          }
+          m_ref[r] = mx2;
+          lp[r] *= alpha[r];
+        }
+      }
+      // P^T buffer j % NPB is free once PV_{j-NPB} completed; O^T is rescaled
+      // (columns of the rows whose reference moved) once PV_{j-1} completed
+      if (j >= NPB)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(pv_done + j % NPB, ((j - NPB) / NPB) & 1, lim, p.status, abort_flag));
+      if (ok && rescale && j > 0) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(pv_done + (j - 1) % NPB, ((j - 1) / NPB) & 1, lim, p.status, abort_flag));
+        if (ok) {
+          tc_fence_after();
+          uint32_t ov[NP];
+          tmem_ld16_dg(tmem + lane_base + C::O_COL, ov);
+          tmem_ld_wait16_dg(ov);
+#pragma unroll
+          for (int r = 0; r < NP; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * alpha[r]);
+          tmem_st16(tmem + lane_base + C::O_COL, ov);
+          tmem_st_wait();
+        }
+      }
+      if (ok) {
+        // P^T_j[r][kr] = 2^(x * sl2 - m_ref), bf16, at row r, key kr of the
+        // K-major layout: box kr / 64, 16-byte chunk (kr % 64) / 8 swizzled
+        // with the row's position in its 8-row group
+        const uint32_t pb = smem_u32(smem + C::P_OFF + (j % NPB) * 2 * C::QBOX) + (kr >> 6) * C::QBOX;
+        const uint32_t chunk = static_cast<uint32_t>((kr & 63) >> 3), within = static_cast<uint32_t>((kr & 7) * 2);
+#pragma unroll
+        for (int r = 0; r < NP; ++r) {
+          const float pr = (m_ref[r] == -INFINITY) ? 0.f : ex2_approx(fmaf(x[r], sl2, -m_ref[r]));  // -inf -> 0
+          lp[r] += pr;
+          const uint32_t addr = pb + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4) + within;
+          st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr)));
+        }
+        fence_proxy_async_smem();  // the tensor core reads P^T through the async proxy
+        tc_fence_before();
+        mbar_arrive(p_full + (j & 1));
+      }
+    }
+    // ---- epilogue: the unnormalised partial (o, m, l) of this split
+    if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_last, 0, lim, p.status, abort_flag));
+    float v[NP];
+#pragma unroll
+    for (int r = 0; r < NP; ++r) v[r] = lp[r];
+    warp_reduce16<false>(v, lane);
+    float* rs = red + 2 * NP * 4;
+    if ((lane & 1) == 0) rs[((lane >> 1) & 15) * 4 + wq] = v[0];
+    ok = bar_and(DGT_BAR_ID, 128, ok);
+    if (ok) {
+      tc_fence_after();
+      uint32_t ov[NP];
+      if (n > 0) {
+        tmem_ld16_dg(tmem + lane_base + C::O_COL, ov);  // O^T row kr = output column d = kr
+        tmem_ld_wait16_dg(ov);
+      } else {
+#pragma unroll
+        for (int r = 0; r < NP; ++r) ov[r] = 0u;
+      }
+      const int g = bg % p.Hkv;
+      float m_mine = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < NP; ++r) {
+        if (r == kr) m_mine = m_ref[r];
+        if (r < p.R) {
+          // query row (b, g * G + r / Nq, r % Nq) of [B, H, Nq]
+          const size_t qrow = (static_cast<size_t>(b) * p.H + g * p.G + r / p.Nq) * p.Nq + r % p.Nq;
+          p.ws_o[(qrow * p.S + s) * DGT_D + kr] = __uint_as_float(ov[r]);
+        }
+      }
+      if (kr < p.R) {
+        const float4 l4 = reinterpret_cast<const float4*>(rs)[kr];
+        const size_t qrow = (static_cast<size_t>(b) * p.H + g * p.G + kr / p.Nq) * p.Nq + kr % p.Nq;
+        const size_t part = qrow * p.S + s;
+        p.ws_ml[part * 2 + 0] = m_mine;
+        p.ws_ml[part * 2 + 1] = (l4.x + l4.y) + (l4.z + l4.w);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == DG_MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 template <int D>
 static cudaError_t launch_decode_grouped_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                            const DecodeGroupedParams& p, cudaStream_t stream) {
@@ -362,16 +800,46 @@ static cudaError_t launch_decode_grouped_t(const CUtensorMap& tq, const CUtensor
   return cudaGetLastError();
 }
 
+#ifndef FA_DGT_NK
+#define FA_DGT_NK 1   // K stages of the keys-on-lanes kernel
+#endif
+#ifndef FA_DGT_NV
+#define FA_DGT_NV 1   // V stages
+#endif
+#ifndef FA_DGT_NPB
+#define FA_DGT_NPB 1  // P^T buffers
+#endif
+#ifndef FA_DGT_MINB
+#define FA_DGT_MINB 3 // CTAs per SM the registers are sized for
+#endif
+#ifndef FA_DGT_ENABLE
+#define FA_DGT_ENABLE 1
+#endif
+using DgtKernel = DgtCfg<FA_DGT_NK, FA_DGT_NV, FA_DGT_NPB>;
+#define FA_DGT_KERNEL fa_decode_grouped_kt_kernel<FA_DGT_NK, FA_DGT_NV, FA_DGT_NPB, FA_DGT_MINB>
+
+// The keys-on-lanes kernel takes d = 128 with at most 16 query rows per K/V head.
+static bool use_kt(int d, int R) { return FA_DGT_ENABLE && d == 128 && R <= DGT_NP; }
+
+int decode_grouped_q_box_rows(int d, int R) { return use_kt(d, R) ? DGT_NP : 128; }
+
 cudaError_t decode_grouped_set_attributes(int d) {
   if (d == 64)
     return cudaFuncSetAttribute(fa_decode_grouped_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 DgCfg<64>::SMEM);
-  return cudaFuncSetAttribute(fa_decode_grouped_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              DgCfg<128>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(fa_decode_grouped_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DgCfg<128>::SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(FA_DGT_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, DgtKernel::SMEM);
 }
 
 cudaError_t launch_decode_grouped(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const DecodeGroupedParams& p, cudaStream_t stream) {
+  if (use_kt(d, p.R)) {
+    const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.S);
+    FA_DGT_KERNEL<<<grid, DGT_THREADS, DgtKernel::SMEM, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+  }
   return d == 64 ? launch_decode_grouped_t<64>(tq, tk, tv, p, stream)
                  : launch_decode_grouped_t<128>(tq, tk, tv, p, stream);
 }

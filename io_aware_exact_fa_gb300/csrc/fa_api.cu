@@ -132,11 +132,12 @@ fa_status device_state(DeviceState** out) {
 // (stores).
 // 3-D tensor map over [BH, rows, d] with 128-byte-swizzled boxes of 128 rows
 // x 128 bytes: 64 bf16 elements, or (e4m3) 128 one-byte codes.
-fa_status encode_map(CUtensorMap* map, const void* base, int rows, int BH, int d, bool e4m3 = false) {
+fa_status encode_map(CUtensorMap* map, const void* base, int rows, int BH, int d, bool e4m3 = false,
+                     int box_rows = 128) {
   const cuuint64_t esz = e4m3 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz, static_cast<cuuint64_t>(rows) * d * esz};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                         const_cast<void*>(base), dims, strides, box,
@@ -536,7 +537,8 @@ fa_status fa_decode_grouped(const void* q, const void* k_cache, const void* v_ca
   if (fa_status s = device_state(&st)) return s;
   const int BHkv = B * Hkv;
   CUtensorMap tq, tk, tv;
-  if (fa_status s = encode_map(&tq, q, G * Nq, BHkv, d)) return s;  // the G*Nq rows of a group are contiguous
+  // the G*Nq rows of a group are contiguous; the box covers the kernel's query tile
+  if (fa_status s = encode_map(&tq, q, G * Nq, BHkv, d, false, fa::decode_grouped_q_box_rows(d, G * Nq))) return s;
   if (fa_status s = encode_map(&tk, k_cache, Nk, BHkv, d)) return s;
   if (fa_status s = encode_map(&tv, v_cache, Nk, BHkv, d)) return s;
   const size_t parts = static_cast<size_t>(rows) * num_splits;
