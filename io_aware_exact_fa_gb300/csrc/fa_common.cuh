@@ -81,6 +81,8 @@ struct PrefillParams {
   int units;                 // work units: Q-tile pairs, then single Q tiles (see split_from)
   unsigned int* dbg;         // debug build: the device check record (FA_DBG_WORDS words); else nullptr
   int split_from;            // units from here on are single tiles of the last pairs
+  int band;                  // causal unit order: 0 = pair-major over all heads; else bands of `band`
+                             // pair lengths (longest first), each band walked head by head
 };
 
 struct BwdParams {

@@ -289,8 +289,22 @@ __device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u, int kv_
     pu = p.split_from + (u - p.split_from) / 2;
     only = (u - p.split_from) & 1;
   }
-  w.pair = p.causal ? (p.n_qpairs - 1 - pu / BH) : (pu / BH);
-  w.bh = pu % BH;
+  if (p.causal && p.band > 0) {
+    // Bands of `band` pair lengths, longest band first; inside a band one
+    // head's pairs (longest first), then the next head's. The CTAs running at
+    // once then read the K/V of about (CTAs / band) heads, which L2 holds,
+    // while the last units launched are still the shortest.
+    const int per_band = p.band * BH;
+    const int bi = pu / per_band;
+    const int r = pu - bi * per_band;
+    const int bw = min(p.band, p.n_qpairs - bi * p.band);  // pairs in this band (the last may be short)
+    const int head = r / bw;
+    w.pair = p.n_qpairs - 1 - (bi * p.band + (r - head * bw));
+    w.bh = head;
+  } else {
+    w.pair = p.causal ? (p.n_qpairs - 1 - pu / BH) : (pu / BH);
+    w.bh = pu % BH;
+  }
   const int nkv_total = (p.Nk + BLOCK_N - 1) / BLOCK_N;
   int n[Q_TILES];
 #pragma unroll
@@ -371,7 +385,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   const bool trim = p.keep != nullptr && p.msq == 0;
 
   if (trim && producer && pw == 3) {
-    const int bh = cta % (p.B * p.H);
+    const int bh = unit_info(p, cta, INT_MAX).bh;  // one unit per CTA here: unit cta
     const int b = bh / p.H, h = bh % p.H;
     const uint32_t* kb = p.keep + b * p.msb + h * p.msh;
     const int nwords = (p.Nk + 31) >> 5;
