@@ -715,7 +715,7 @@ def main():
     ap.add_argument("--prefill-h", type=int, default=0, help="override the prefill heads (profiling a small case)")
     ap.add_argument("--dv-b", type=int, default=0, help="override the decode-variant batch (profiling a small case)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--no-fp8", action="store_true", help="skip the e4m3-input legs of the long-context workloads")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the e4m3-input legs (the headline and long-context workloads)")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the long-context prefill legs (8k and 32k, d=128; reported under 'long_context')")
     ap.add_argument("--e2e-chunk-heads", type=int, default=0,
@@ -827,6 +827,11 @@ def main():
     dvar = run_decode_variants(args, fa, W, stream, warm, world, rank, dev) if do_v else None
     mat = run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, dev) if do_m else None
     lng = run_long_context(args, fa, W, flush, stream, warm, world, rank, dev) if do_l else None
+    # the headline workload on e4m3 inputs, both modes of the step
+    pf8 = None
+    if do_p and not args.no_fp8 and not wp.pad_heads:
+        pf8 = {"modes": {("causal" if c else "noncausal"): run_fp8(args, fa, W, wp, c, flush, stream, warm, world,
+                                                                   rank, dev) for c in modes}}
     sampler.stop()
     clocks = sampler.summary((t_wall0, t_wall1))
     if bwd is not None:
@@ -835,6 +840,18 @@ def main():
         dvar["clocks"] = sampler.summary(dvar.pop("_window"))
     if mat is not None:
         mat["clocks"] = sampler.summary(mat.pop("_window"))
+    if pf8 is not None:
+        for rec in pf8["modes"].values():
+            rec["clocks"] = sampler.summary(rec.pop("_window"))
+        fl = sum(wp.flops(c) for c in modes)
+        ms = sum(r["ms"] for r in pf8["modes"].values())
+        pf8["value"] = fl / (ms / 1e3) / 1e12 * world
+        pf8["unit"] = "TFLOP/s"
+        pf8["workload"] = wp.name + " (" + " + ".join(pf8["modes"]) + "), e4m3 inputs"
+        pk = next(iter(pf8["modes"].values()))["roofline"]["peak"]
+        pf8["roofline"] = {"bound": "tensor", "achieved": fl / (ms / 1e3) / 1e12, "peak": pk, "unit": "TFLOP/s",
+                           "frac": fl / (ms / 1e3) / 1e12 / pk, "kernel": f"fa_prefill_kernel<{wp.d}, e4m3>",
+                           "peak_source": "measured bf16 burst x 2 (nominal fp8 / bf16 dense ratio)"}
     if lng is not None:
         for rec in lng["workloads"].values():
             rec["clocks"] = sampler.summary(rec.pop("_window"))
@@ -972,6 +989,8 @@ def main():
             mat["fused_speedup"] = {("causal" if c else "noncausal"): tmm / tm
                                     for c, tm, tmm in zip(modes, t_modes, t_mat)}
         line["materialized"] = mat
+    if pf8 is not None:
+        line["prefill_fp8"] = pf8
     if lng is not None:
         line["long_context"] = lng
         if not do_p and not do_d and bwd is None and dvar is None:

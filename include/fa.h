@@ -107,7 +107,7 @@ fa_status fa_fwd_masked(const void* q, const void* k, const void* v, void* o, fl
  * The score and value products run on the tensor cores in e4m3 with fp32
  * accumulation; P is rounded to e4m3 (round to nearest even) before the P V
  * product, which is this path's main error against the exact result.
- * Supported: d = 128 (FA_ERR_UNSUPPORTED otherwise); no key mask. Errors as
+ * Supported: d = 64 or 128 (FA_ERR_UNSUPPORTED otherwise); no key mask. Errors as
  * for fa_fwd, plus FA_ERR_INVALID_ARG for a descale that is not finite and
  * positive, or a product scale * descale_q * descale_k that overflows. */
 fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -104,6 +104,8 @@ fa_status device_state(DeviceState** out) {
       return cuda_fail(e, "cudaFuncSetAttribute(d=128)");
     if ((e = fa::prefill_set_attributes(128, true)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(e4m3 d=128)");
+    if ((e = fa::prefill_set_attributes(64, true)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(e4m3 d=64)");
     if ((e = fa::bwd_set_attributes(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=64)");
     if ((e = fa::bwd_set_attributes(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd d=128)");
     if ((e = fa::materialized_set_attributes()) != cudaSuccess)
@@ -114,9 +116,9 @@ fa_status device_state(DeviceState** out) {
       return cuda_fail(e, "cudaFuncSetAttribute(grouped decode d=128)");
     // The in-kernel register split assumes this launch allocation; a
     // different one could make setmaxnreg.inc wait forever, so refuse.
-    for (int v = 0; v < 3; ++v) {
-      const int d = v == 0 ? 64 : 128;
-      const bool f8 = v == 2;
+    for (int v = 0; v < 4; ++v) {
+      const int d = (v & 1) ? 128 : 64;
+      const bool f8 = v >= 2;
       const int regs = fa::prefill_num_regs(d, f8);
       if (regs != fa::prefill_launch_regs(d))
         return fail(FA_ERR_UNSUPPORTED, "prefill kernel (d=%d%s) built with %d registers, expected %d", d,
@@ -146,11 +148,14 @@ fa_status encode_map(CUtensorMap* map, const void* base, int rows, int BH, int d
   const cuuint64_t esz = e4m3 ? 1 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz, static_cast<cuuint64_t>(rows) * d * esz};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows), 1};
+  // a box row is 128 bytes (128-byte swizzle), or the whole 64-byte row of an
+  // e4m3 tensor with d = 64 (64-byte swizzle)
+  const cuuint64_t row_bytes = std::min<cuuint64_t>(static_cast<cuuint64_t>(d) * esz, 128);
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(row_bytes / esz), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                        const_cast<void*>(base), dims, strides, box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
   return FA_OK;
@@ -274,7 +279,7 @@ fa_status prefill_common(const void* q, const void* k, const void* v, void* o, f
     for (float x : {f8.dq, f8.dk, f8.dv})
       if (!std::isfinite(x) || !(x > 0.f)) return fail(FA_ERR_INVALID_ARG, "descale factors must be finite and > 0");
     if (!std::isfinite(scale * f8.dq * f8.dk)) return fail(FA_ERR_INVALID_ARG, "scale * descale_q * descale_k overflows");
-    if (d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported for e4m3 inputs (128)", d);
+    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported for e4m3 inputs (64 or 128)", d);
   }
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
   if (Nq == 0) return FA_OK;  // nothing to compute (an empty q may have a NULL data pointer)

@@ -173,6 +173,11 @@ __device__ __forceinline__ void tc_fence_after() {
 __host__ __device__ constexpr uint32_t sdesc_sw128_hi(uint32_t sbo_bytes) {
   return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
+// High word of a descriptor for 64-byte-swizzled tiles (rows of 64 bytes,
+// 8-row groups sbo_bytes apart: 512 for a dense tile), layout type 4.
+__host__ __device__ constexpr uint32_t sdesc_sw64_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (4u << 29);
+}
 __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }

@@ -103,17 +103,22 @@ namespace fa {
 template <int D, bool F8 = false>
 struct PrefillCfg {
   static_assert(D == 64 || D == 128, "head dim 64 or 128");
-  static_assert(!F8 || D == 128, "the e4m3 path is built for d = 128");
   static constexpr int ESZ = F8 ? 1 : 2;              // bytes per q, k, v element
   static constexpr int TILE_BYTES = BLOCK_N * D * ESZ;  // one Q, K or V tile (128 rows x D elements)
-  static constexpr int BOX_BYTES = 128 * 128;         // one TMA box: 128 rows x 128 bytes
-  static constexpr int BOX_ELEMS = 128 / ESZ;         // elements per box row (64 bf16 or 128 e4m3)
+  // Shared-memory rows of a tile are 128 bytes (128-byte swizzle), except the
+  // e4m3 tiles at d = 64, whose 64-byte rows use the 64-byte swizzle.
+  static constexpr int ROW_BYTES = (D * ESZ < 128) ? D * ESZ : 128;
+  static constexpr int BOX_BYTES = 128 * ROW_BYTES;   // one TMA box: 128 rows
+  static constexpr int BOX_ELEMS = ROW_BYTES / ESZ;   // elements per box row (64 bf16, 128 or 64 e4m3)
   static constexpr int NBOX = D / BOX_ELEMS;
+  // high word of every operand descriptor: 8-row groups of ROW_BYTES rows
+  static constexpr uint32_t DESC_HI = (ROW_BYTES == 64) ? sdesc_sw64_hi(512) : sdesc_sw128_hi(1024);
   static constexpr int O_TILE_BYTES = BLOCK_M * D * 2;  // one bf16 O tile
   static constexpr int NBOX_O = D / 64;
+  static constexpr int O_BOX_BYTES = 128 * 128;       // one box of the bf16 O tile: 128 rows x 64 bf16
   // products: one K-step takes 32 bytes of every A and B row (16 bf16 or 32
   // e4m3 elements); S = Q K^T has D * ESZ / 32 of them, O += P V has
-  // BLOCK_N * ESZ / 32 (each K-step of V is PV_KROWS rows of 128 bytes)
+  // BLOCK_N * ESZ / 32 (each K-step of V is PV_KROWS rows of ROW_BYTES bytes)
   static constexpr int KSTEPS_S = D * ESZ / 32;
   static constexpr int KSTEPS_PV = BLOCK_N * ESZ / 32;
   static constexpr int PV_KROWS = 32 / ESZ;
@@ -541,7 +546,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       // K-step kk of Q and K (K-major) starts (kk / 4) boxes plus (kk % 4) x 32
       // bytes in; that of V (MN-major, 64-column boxes LBO apart) 16 rows =
       // 2048 bytes in. Another ring slot adds its offset to the low word.
-      constexpr uint32_t DHI = sdesc_sw128_hi(1024);
+      constexpr uint32_t DHI = C::DESC_HI;
       const uint32_t q_lo = sdesc_sw128_lo(sQa, 16);
       const uint32_t k_lo = sdesc_sw128_lo(smem_u32(sK), 16);
       const uint32_t v_lo = sdesc_sw128_lo(smem_u32(sV), C::BOX_BYTES);
@@ -635,7 +640,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
 #pragma unroll
           for (int kk = 0; kk < C::KSTEPS_PV; ++kk) {
             // A: 8 TMEM columns (32 bytes of P per row) per K-step; B: PV_KROWS rows of V
-            const uint32_t vk = vb + static_cast<uint32_t>((kk * C::PV_KROWS * 128) >> 4);
+            const uint32_t vk = vb + static_cast<uint32_t>((kk * C::PV_KROWS * C::ROW_BYTES) >> 4);
             if (!dbg_tmem_mma_ok(p.dbg, DBG_MMA_PV, dO, D, aP + kk * 8, 8)) continue;
             if (issuer()) {
               if constexpr (F8) mma_ts_w_f8(dO, aP + kk * 8, vk, DHI, C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
@@ -962,7 +967,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int c = ch * 4 + v;  // 16-byte chunk of the row: box c / 8, chunk c % 8 of the box
-            const uint32_t a = srow + static_cast<uint32_t>((c >> 3) * C::BOX_BYTES) +
+            const uint32_t a = srow + static_cast<uint32_t>((c >> 3) * C::O_BOX_BYTES) +
                                (static_cast<uint32_t>((c & 7) ^ (row & 7)) << 4);
             st_shared_v4(a, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
@@ -978,7 +983,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
 #pragma unroll
           for (int b = 0; b < C::NBOX_O; ++b)
             if (dbg_tma_ok(p.dbg, DBG_STORE_O, 64 * b, r0, bh, D, p.Nq, p.B * p.H, 2))
-              tma_store_3d(&tmO, sO + b * C::BOX_BYTES, 64 * b, r0, bh);
+              tma_store_3d(&tmO, sO + b * C::O_BOX_BYTES, 64 * b, r0, bh);
           bulk_commit_group();
           bulk_wait_group_read_all();
         }
@@ -1050,33 +1055,37 @@ static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk
   return cudaGetLastError();
 }
 
-// The instantiations: bf16 at d = 64 and 128, e4m3 at d = 128.
-int prefill_num_regs(int d, bool f8) {
+// The instantiations: bf16 and e4m3, each at d = 64 and 128.
+template <int D, bool F8>
+static int num_regs_t() {
   cudaFuncAttributes a{};
-  const cudaError_t e = f8        ? cudaFuncGetAttributes(&a, fa_prefill_kernel<128, true>)
-                        : d == 64 ? cudaFuncGetAttributes(&a, fa_prefill_kernel<64, false>)
-                                  : cudaFuncGetAttributes(&a, fa_prefill_kernel<128, false>);
-  return e == cudaSuccess ? a.numRegs : -1;
+  return cudaFuncGetAttributes(&a, fa_prefill_kernel<D, F8>) == cudaSuccess ? a.numRegs : -1;
+}
+int prefill_num_regs(int d, bool f8) {
+  if (f8) return d == 64 ? num_regs_t<64, true>() : num_regs_t<128, true>();
+  return d == 64 ? num_regs_t<64, false>() : num_regs_t<128, false>();
 }
 
 size_t prefill_smem_bytes(int d, bool f8) {
-  return f8 ? PrefillCfg<128, true>::SMEM : d == 64 ? PrefillCfg<64>::SMEM : PrefillCfg<128>::SMEM;
+  if (f8) return d == 64 ? PrefillCfg<64, true>::SMEM : PrefillCfg<128, true>::SMEM;
+  return d == 64 ? PrefillCfg<64>::SMEM : PrefillCfg<128>::SMEM;
 }
 
+template <int D, bool F8>
+static cudaError_t set_attributes_t() {
+  return cudaFuncSetAttribute(fa_prefill_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PrefillCfg<D, F8>::SMEM);
+}
 cudaError_t prefill_set_attributes(int d, bool f8) {
-  if (f8)
-    return cudaFuncSetAttribute(fa_prefill_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                PrefillCfg<128, true>::SMEM);
-  if (d == 64)
-    return cudaFuncSetAttribute(fa_prefill_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                PrefillCfg<64>::SMEM);
-  return cudaFuncSetAttribute(fa_prefill_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              PrefillCfg<128>::SMEM);
+  if (f8) return d == 64 ? set_attributes_t<64, true>() : set_attributes_t<128, true>();
+  return d == 64 ? set_attributes_t<64, false>() : set_attributes_t<128, false>();
 }
 
 cudaError_t launch_prefill(int d, bool f8, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& to, const PrefillParams& p, cudaStream_t stream) {
-  if (f8) return launch_prefill_t<128, true>(tq, tk, tv, to, p, stream);
+  if (f8)
+    return d == 64 ? launch_prefill_t<64, true>(tq, tk, tv, to, p, stream)
+                   : launch_prefill_t<128, true>(tq, tk, tv, to, p, stream);
   return d == 64 ? launch_prefill_t<64, false>(tq, tk, tv, to, p, stream)
                  : launch_prefill_t<128, false>(tq, tk, tv, to, p, stream);
 }

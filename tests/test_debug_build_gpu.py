@@ -121,13 +121,14 @@ def test_debug_build_clean_and_identical(libs, case):
     assert torch.equal(o_d, o_r) and torch.equal(l_d, l_r)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("Nq,Nk,causal", [(200, 300, True), (513, 129, True), (1, 700, False)])
-def test_debug_build_fp8_clean_and_identical(libs, Nq, Nk, causal):
+def test_debug_build_fp8_clean_and_identical(libs, Nq, Nk, causal, d):
     fa, rel, dbg = libs
-    (q8, k8, v8), ds = W.make_qkv_fp8(2, 2, Nq, Nk, 128, seed=Nq + Nk, device="cuda")
+    (q8, k8, v8), ds = W.make_qkv_fp8(2, 2, Nq, Nk, d, seed=Nq + Nk, device="cuda")
     _record(dbg)
-    o_d, l_d = _fwd8(dbg, q8, k8, v8, ds, 1 / math.sqrt(128), causal)
+    o_d, l_d = _fwd8(dbg, q8, k8, v8, ds, 1 / math.sqrt(d), causal)
     rec = _record(dbg)
     assert rec == [0] * 8, f"debug checks failed: {rec}"
-    o_r, l_r = _fwd8(rel, q8, k8, v8, ds, 1 / math.sqrt(128), causal)
+    o_r, l_r = _fwd8(rel, q8, k8, v8, ds, 1 / math.sqrt(d), causal)
     assert torch.equal(o_d, o_r) and torch.equal(l_d, l_r)

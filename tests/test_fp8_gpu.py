@@ -73,11 +73,11 @@ CASES = [  # B, H, Nq, Nk, causal, scale
 ]
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("case", CASES, ids=[f"b{c[0]}h{c[1]}q{c[2]}k{c[3]}{'c' if c[4] else ''}"
                                              f"{'neg' if c[5] and c[5] < 0 else ''}" for c in CASES])
-def test_fp8_parity_every_element(fa, case):
+def test_fp8_parity_every_element(fa, case, d):
     B, H, Nq, Nk, causal, scale = case
-    d = 128
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     (q8, k8, v8), ds = W.make_qkv_fp8(B, H, Nq, Nk, d, seed=Nq + 7 * Nk + H)
     o, lse = run(fa, q8, k8, v8, ds, scale, causal)
@@ -109,18 +109,39 @@ def test_fp8_long_context_sampled(fa):
         print(h, check(to64(o[0, h][sel]), to64(lse[0, h][sel]), ro, rl, vmax, f"8k head {h}"))
 
 
+def test_fp8_headline_sampled(fa):
+    """B=4 H=16 N=2048 d=64 (the headline prefill workload), both causal modes,
+    on e4m3 inputs: three whole heads and 256 seeded rows of three more."""
+    B, H, N, d = 4, 16, 2048, 64
+    scale = 1.0 / math.sqrt(d)
+    (q8, k8, v8), ds = W.make_qkv_fp8(B, H, N, N, d, seed=0, device="cuda")
+    rows = np.unique(np.concatenate([W.sample_rows(N, 256, seed=11).numpy(), [0, N - 1]]))
+    for causal in (False, True):
+        o, lse = fa.fwd_fp8(q8, k8, v8, *ds, scale=scale, causal=causal)
+        torch.cuda.synchronize()
+        assert fa.device_status() == fa.FA_OK
+        for (b, h), rr in [((0, 0), None), ((3, 15), None), ((2, 7), None), ((1, 3), rows), ((2, 9), rows),
+                           ((3, 1), rows)]:
+            qh, kh, vh = (t[b, h].cpu().numpy() for t in (q8, k8, v8))
+            ro, rl = FP8.attend_head_fp8(qh, kh, vh, *ds, scale, causal, rows=rr)
+            sel = slice(None) if rr is None else rr
+            vmax = np.abs(FP8.dequantize(vh, ds[2])).max()
+            check(to64(o[b, h][sel]), to64(lse[b, h][sel]), ro, rl, vmax, f"2k d64 causal={causal} ({b},{h})")
+
+
 def test_fp8_deterministic(fa):
-    (q8, k8, v8), ds = W.make_qkv_fp8(2, 4, 1000, 1000, 128, seed=9, device="cuda")
-    a = fa.fwd_fp8(q8, k8, v8, *ds, causal=True)
-    b = fa.fwd_fp8(q8, k8, v8, *ds, causal=True)
-    torch.cuda.synchronize()
-    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    for d in (64, 128):
+        (q8, k8, v8), ds = W.make_qkv_fp8(2, 4, 1000, 1000, d, seed=9, device="cuda")
+        a = fa.fwd_fp8(q8, k8, v8, *ds, causal=True)
+        b = fa.fwd_fp8(q8, k8, v8, *ds, causal=True)
+        torch.cuda.synchronize()
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
 def test_fp8_rejects_bad_arguments(fa):
-    q8 = torch.zeros(1, 1, 128, 64, dtype=torch.uint8, device="cuda")
+    q8 = torch.zeros(1, 1, 128, 96, dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FAError) as e:
-        fa.fwd_fp8(q8, q8, q8, 1.0, 1.0, 1.0)          # d = 64: not built for e4m3
+        fa.fwd_fp8(q8, q8, q8, 1.0, 1.0, 1.0)          # d = 96: not built
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
     q8 = torch.zeros(1, 1, 128, 128, dtype=torch.uint8, device="cuda")
     for bad in ((0.0, 1.0, 1.0), (1.0, float("nan"), 1.0), (1.0, 1.0, -2.0)):
