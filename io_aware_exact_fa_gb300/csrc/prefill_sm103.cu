@@ -52,6 +52,9 @@ namespace fa {
 #ifndef FA_EMU_PAIRS_D128
 #define FA_EMU_PAIRS_D128 0
 #endif
+#ifndef FA_LATE_STORE_WAIT
+#define FA_LATE_STORE_WAIT 1   // O staging: wait for the previous store's reads only before rewriting the buffer
+#endif
 #ifndef FA_STAGGER_D64
 #define FA_STAGGER_D64 1
 #endif
@@ -939,6 +942,15 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       // itself is waited for. Rows are written in the 128-byte-swizzled layout
       // the tensor map expects; rows past Nq are clipped by the store. Once the
       // store has read the buffer (q_free) the next Q may be loaded into it.
+      // With separate O staging the previous unit's store must have read the
+      // buffer before it is rewritten: the storer waits for that here, where
+      // the store has long finished, rather than right after issuing it,
+      // where the wait would delay its warp's first softmax step of the next
+      // unit.
+      if (C::O_STAGE && FA_LATE_STORE_WAIT) {
+        if (storer) bulk_wait_group_read_all();
+        named_bar_sync(1 + t, 128);
+      }
       if (ok && active && (n > 0 || !C::O_STAGE)) {
         ok = (n > 0) ? mbar_wait(o_done + t, static_cast<uint32_t>((ct + n - 1) & 1), lim, p.status, abort_flag)
                      : mbar_wait(q_full + t, k & 1, lim, p.status, abort_flag);
@@ -985,7 +997,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             if (dbg_tma_ok(p.dbg, DBG_STORE_O, 64 * b, r0, bh, D, p.Nq, p.B * p.H, 2))
               tma_store_3d(&tmO, sO + b * C::O_BOX_BYTES, 64 * b, r0, bh);
           bulk_commit_group();
-          bulk_wait_group_read_all();
+          if (!(C::O_STAGE && FA_LATE_STORE_WAIT)) bulk_wait_group_read_all();
         }
         if (!C::O_STAGE) mbar_arrive(q_free + t);
       }
