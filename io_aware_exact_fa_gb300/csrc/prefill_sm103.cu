@@ -55,6 +55,12 @@ namespace fa {
 #ifndef FA_LATE_STORE_WAIT
 #define FA_LATE_STORE_WAIT 1   // O staging: wait for the previous store's reads only before rewriting the buffer
 #endif
+#ifndef FA_QDB_D64
+#define FA_QDB_D64 1           // two Q buffers per tile at d = 64
+#endif
+#ifndef FA_QDB_RING
+#define FA_QDB_RING 4          // K and V ring slots beside them (bf16)
+#endif
 #ifndef FA_STAGGER_D64
 #define FA_STAGGER_D64 1
 #endif
@@ -130,11 +136,17 @@ struct PrefillCfg {
   // K_{j+1} can land while P_j is still being computed. Both slots of key
   // tile j are released together, by one release barrier per tile that both
   // issuers signal once their MMAs reading tile j have completed.
-  static constexpr int NK = (D == 128 && !F8) ? 3 : 4;  // K ring slots
-  static constexpr int NV = (D == 128 && !F8) ? 2 : 4;  // V ring slots
+  // At d = 64 each Q tile has two buffers (QDB): unit k's Q goes to buffer
+  // k % 2, so it loads while unit k - 1 runs instead of after unit k - 1's
+  // last score product. (Measured: e4m3 +0.5 % / +2 % non-causal / causal,
+  // bf16 flat; with the bf16 K and V rings cut to three slots, causal -3 %.)
+  static constexpr bool QDB = (D == 64) && FA_QDB_D64;
+  static constexpr int QB = QDB ? 2 : 1;                // Q buffers per tile
+  static constexpr int NK = (D == 128 && !F8) ? 3 : ((QDB && !F8) ? FA_QDB_RING : 4);  // K ring slots
+  static constexpr int NV = (D == 128 && !F8) ? 2 : ((QDB && !F8) ? FA_QDB_RING : 4);  // V ring slots
   static constexpr int NR = NK > NV ? NK : NV;        // release barriers (tile j uses j % NR)
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_TILES * TILE_BYTES;
+  static constexpr int Q_OFF = 0;                     // Q of tile t, buffer b at Q_OFF + (b Q_TILES + t) TILE_BYTES
+  static constexpr int K_OFF = QB * Q_TILES * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + NK * TILE_BYTES;
   // At d = 64 the epilogue stages O in buffers of its own, so the next unit's
   // Q may be loaded as soon as this unit's score MMAs are done; at d = 128
@@ -143,6 +155,7 @@ struct PrefillCfg {
   static constexpr bool O_STAGE = ((D == 64) && FA_O_STAGE) || F8;
   static constexpr int O_OFF = V_OFF + NV * TILE_BYTES;
   static constexpr int BAR_OFF = O_OFF + (O_STAGE ? Q_TILES * O_TILE_BYTES : 0);
+  static_assert(!QDB || O_STAGE, "two Q buffers need O staged apart (the epilogue would stage O in buffer 0)");
   // TMEM columns: S_0 [0,128), S_1 [128,256), O_t at O_COL + D*t; with
   // SEP_P (d = 64) P_t gets its own 64 columns at P_COL + 64*t, otherwise P_t
   // overwrites the first P_WORDS columns of S_t. P is packed 4 / ESZ values
@@ -153,7 +166,7 @@ struct PrefillCfg {
   static constexpr uint32_t P_COL = SEP_P ? O_COL + Q_TILES * D : 0;
   static constexpr uint32_t P_STRIDE = SEP_P ? P_WORDS : BLOCK_N;
   static_assert(!SEP_P || P_COL + Q_TILES * P_WORDS <= 512, "TMEM budget");
-  static constexpr int NBAR = 6 * Q_TILES + NK + NV + NR + 2;
+  static constexpr int NBAR = 6 * Q_TILES + 2 * (QB - 1) * Q_TILES + NK + NV + NR + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;   // + slack to align the base to 1024
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -356,10 +369,12 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   uint8_t* sK = smem + C::K_OFF;
   uint8_t* sV = smem + C::V_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* q_full = bars;                 // Q_t of unit k landed (phase k)
-  uint64_t* q_free = q_full + Q_TILES;     // Q_t buffer free again after unit k (phase k): its score
-                                           // MMAs are done (O_STAGE) or its O store read it
-  uint64_t* full_k = q_free + Q_TILES;     // K of key tile g landed in slot g % NK
+  // Q barriers of tile t, buffer b at QB t + b; unit k uses buffer k % QB
+  // in phase k / QB (qbuf, qpar below)
+  uint64_t* q_full = bars;                     // Q_t of unit k landed
+  uint64_t* q_free = q_full + C::QB * Q_TILES; // Q_t buffer free again after unit k: its score MMAs are
+                                               // done (O_STAGE) or its O store read it
+  uint64_t* full_k = q_free + C::QB * Q_TILES; // K of key tile g landed in slot g % NK
   uint64_t* full_v = full_k + NK;          // V of key tile g landed in slot g % NV
   uint64_t* rel = full_v + NV;             // both issuers are done with key tile g (g % NR)
   uint64_t* s_full = rel + NR;             // S_t of step c complete (per-tile step count c)
@@ -407,8 +422,10 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < Q_TILES; ++t) {
-      mbar_init(q_full + t, 1);
-      mbar_init(q_free + t, 1);
+      for (int b = 0; b < C::QB; ++b) {
+        mbar_init(q_full + C::QB * t + b, 1);
+        mbar_init(q_free + C::QB * t + b, 1);
+      }
       mbar_init(s_full + t, 1);
       mbar_init(p_full + t, 128);
       mbar_init(o_done + t, 1);
@@ -434,6 +451,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   // Every role walks the same unit sequence; barrier phases run on across
   // units (counts of units, key tiles and per-tile steps done so far).
   auto unit_at = [&](int k) { return unit_of(cta, k, G, snake); };
+  auto qbuf = [](int k) { return C::QB == 2 ? (k & 1) : 0; };                              // Q buffer of unit k
+  auto qpar = [](int k) { return static_cast<uint32_t>((C::QB == 2 ? (k >> 1) : k) & 1); };  // its phase parity
   int dbg_count0 = 0, dbg_count1 = 0;  // debug build: steps of a tile (softmax) / K and V loads (producer)
 
   if (producer) {
@@ -503,34 +522,39 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         if (u >= U) break;
         const Unit w = unit_info(p, u, kv_keep);
         for (int t = 0; t < Q_TILES && ok; ++t) {
-          if (k > 0) {
-            // the buffer is free, and this warp's previous load into it has
-            // landed (nobody else waits for it when that tile had no key
-            // tile): a second expect_tx must not join an unfinished phase
-            ok = mbar_wait2(q_free + t, (k - 1) & 1, q_full + t, (k - 1) & 1, lim, p.status, abort_flag);
+          uint64_t* qf = q_full + C::QB * t + qbuf(k);
+          if (k >= C::QB) {
+            // the buffer is free (unit k - QB is done with it), and this
+            // warp's previous load into it has landed (nobody else waits for
+            // it when that tile had no key tile): a second expect_tx must not
+            // join an unfinished phase
+            ok = mbar_wait2(q_free + C::QB * t + qbuf(k), qpar(k - C::QB), qf, qpar(k - C::QB), lim, p.status,
+                            abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
           }
           if (leader) {
             if (t ? w.act1 : w.act0) {
-              mbar_arrive_expect_tx(q_full + t, C::TILE_BYTES);
+              mbar_arrive_expect_tx(qf, C::TILE_BYTES);
               // (the second tile of the last pair may start past Nq: it then
               // reads zeros and computes nothing; the pair grid bounds it)
               for (int b = 0; b < C::NBOX; ++b)
                 if (dbg_tma_ok(p.dbg, DBG_LOAD_Q, C::BOX_ELEMS * b, w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh,
                                D, p.n_qpairs * Q_TILES * BLOCK_M, p.B * p.H, C::ESZ))
-                  tma_load_3d(sQ + t * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, q_full + t, C::BOX_ELEMS * b,
-                              w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh);
+                  tma_load_3d(sQ + (qbuf(k) * Q_TILES + t) * C::TILE_BYTES + b * C::BOX_BYTES, &tmQ, qf,
+                              C::BOX_ELEMS * b, w.pair * (Q_TILES * BLOCK_M) + t * BLOCK_M, w.bh);
             } else {
-              mbar_arrive(q_full + t);  // a tile this unit does not compute: the phase completes empty
+              mbar_arrive(qf);  // a tile this unit does not compute: the phase completes empty
             }
           }
           ++issued[t];
         }
       }
       if (!ok && leader) {
+        // error path: the last loads into each buffer land before the CTA exits
         for (int t = 0; t < Q_TILES; ++t)
-          if (issued[t] > 0) mbar_wait_drain(q_full + t, (issued[t] - 1) & 1, lim);
+          for (int k = max(0, issued[t] - C::QB); k < issued[t]; ++k)
+            mbar_wait_drain(q_full + C::QB * t + qbuf(k), qpar(k), lim);
       }
       __syncwarp();
     } else {
@@ -543,7 +567,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       // warp runs it, votes on every wait, and the lane elect.sync picks
       // issues the MMAs and commits (ELECT_ISSUE).
       const int t = pw - 1;
-      const uint32_t sQa = smem_u32(sQ) + t * C::TILE_BYTES;
+      const uint32_t sQa = smem_u32(sQ) + t * C::TILE_BYTES;  // buffer 0; buffer b is b Q_TILES tiles further
       // Low descriptor words of Q_t, K slot 0 and V slot 0 (every operand
       // shares the high word: 1024-byte 8-row groups, 128-byte swizzle). The
       // K-step kk of Q and K (K-major) starts (kk / 4) boxes plus (kk % 4) x 32
@@ -611,8 +635,10 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         // unit k-1). A tile without key tiles releases its Q buffer only after
         // that: otherwise q_free_t could run two phases ahead of the Q
         // producer's parity wait on it.
-        if (!wait_bar(q_full + t, k & 1)) break;
-        if (nt == 0 && C::O_STAGE && lane == 0) mbar_arrive(q_free + t);
+        if (!wait_bar(q_full + C::QB * t + qbuf(k), qpar(k))) break;
+        if (nt == 0 && C::O_STAGE && lane == 0) mbar_arrive(q_free + C::QB * t + qbuf(k));
+        // Q_t of this unit (descriptor low word)
+        const uint32_t q_lo_u = q_lo + static_cast<uint32_t>((qbuf(k) * Q_TILES * C::TILE_BYTES) >> 4);
 
         auto fk_bar = [&](int jj) { return full_k + ((g0 + jj) % NK); };
         auto fk_par = [&](int jj) { return static_cast<uint32_t>(((g0 + jj) / NK) & 1); };
@@ -625,15 +651,15 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             const uint32_t off = static_cast<uint32_t>(((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4);
             if (!dbg_tmem_mma_ok(p.dbg, DBG_MMA_S, dS, BLOCK_N, 0u, 0)) continue;
             if (issuer()) {
-              if constexpr (F8) mma_ss_w_f8(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
-              else mma_ss_w(dS, q_lo + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
+              if constexpr (F8) mma_ss_w_f8(dS, q_lo_u + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
+              else mma_ss_w(dS, q_lo_u + off, DHI, kb + off, DHI, idesc_s, kk > 0 ? 1u : 0u);
             }
           }
           if (issuer()) mma_commit(s_full + t);
           // the unit's last score MMA: Q_t is free once it (and all before it)
           // completed, and the other issuer may start the next unit
           if (jj == nt - 1) {
-            if (C::O_STAGE && issuer()) mma_commit(q_free + t);
+            if (C::O_STAGE && issuer()) mma_commit(q_free + C::QB * t + qbuf(k));
             if (C::UNIT_DONE_EARLY && issuer()) mma_commit(unit_done);
           }
           issued_any = true;
@@ -953,7 +979,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       }
       if (ok && active && (n > 0 || !C::O_STAGE)) {
         ok = (n > 0) ? mbar_wait(o_done + t, static_cast<uint32_t>((ct + n - 1) & 1), lim, p.status, abort_flag)
-                     : mbar_wait(q_full + t, k & 1, lim, p.status, abort_flag);
+                     : mbar_wait(q_full + C::QB * t + qbuf(k), qpar(k), lim, p.status, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
       }
@@ -999,7 +1025,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
           bulk_commit_group();
           if (!(C::O_STAGE && FA_LATE_STORE_WAIT)) bulk_wait_group_read_all();
         }
-        if (!C::O_STAGE) mbar_arrive(q_free + t);
+        if (!C::O_STAGE) mbar_arrive(q_free + C::QB * t + qbuf(k));
       }
       ct += n;
     }
