@@ -40,6 +40,9 @@ namespace fa {
 #ifndef FA_BWD_ELECT_ISSUE
 #define FA_BWD_ELECT_ISSUE 1
 #endif
+#ifndef FA_BWD_EARLY_S
+#define FA_BWD_EARLY_S 1
+#endif
 
 namespace {
 
@@ -73,8 +76,13 @@ struct BwdCfg {
   static constexpr int V_OFF = K_OFF + TILE_BYTES;
   static constexpr int Q_OFF = V_OFF + TILE_BYTES;                 // 2 stages of (Q, dO)
   static constexpr int DS_OFF = Q_OFF + 2 * 2 * TILE_BYTES;        // NDS dS^T buffers
-  static constexpr int STAT_OFF = DS_OFF + NDS * DS_BYTES;         // lse2[128], Dv[128]
-  static constexpr int BAR_OFF = STAT_OFF + 2 * 128 * 4;
+  // At d = 64 the next step's S^T and dP^T are issued as soon as the
+  // softmax-grad has loaded this step's (EARLY_S), so two steps' statistics
+  // can be live at once: they alternate between two buffers.
+  static constexpr bool EARLY_S = SEP && FA_BWD_EARLY_S;
+  static constexpr int NSTAT = EARLY_S ? 2 : 1;
+  static constexpr int STAT_OFF = DS_OFF + NDS * DS_BYTES;         // [NSTAT] of lse2[128], Dv[128]
+  static constexpr int BAR_OFF = STAT_OFF + NSTAT * 2 * 128 * 4;
   static constexpr int NBAR = 16;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
@@ -186,11 +194,13 @@ __global__ void __launch_bounds__(256) fa_bwd_finish_kernel(const float* __restr
 // offload the MUFU unit. before_math() is called once, after the first TMEM
 // loads are issued and before the statistics are read; before_pstore() once,
 // before the first P^T store; before_store() once, before the first
-// shared-memory store. If any returns false the step stops there.
+// shared-memory store. If any returns false the step stops there. A non-null
+// loaded_bar is arrived on once this thread has loaded all its S^T and dP^T
+// columns.
 template <int D, bool MASK, typename F, typename G, typename E>
 __device__ __forceinline__ bool sg_half(uint32_t tST, uint32_t tDPT, uint32_t tPT, uint32_t ds_row, int row, int h,
                                         int c_lo, const float* nlse2, const float* ndrow, float sl2, G&& before_math,
-                                        E&& before_pstore, F&& before_store) {
+                                        E&& before_pstore, F&& before_store, uint64_t* loaded_bar) {
   using C = BwdCfg<D>;
   const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
@@ -206,6 +216,12 @@ __device__ __forceinline__ bool sg_half(uint32_t tST, uint32_t tDPT, uint32_t tP
     }
     tmem_ld_wait32(sv);
     reg_fence32(dp);
+    if (cc == 1 && loaded_bar != nullptr) {
+      // this thread's S^T and dP^T columns are in registers: the next step's
+      // products may overwrite them
+      tc_fence_before();
+      mbar_arrive(loaded_bar);
+    }
     uint32_t pk[16], dk[16];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -271,8 +287,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint8_t* sV = smem + C::V_OFF;
   uint8_t* sQ0 = smem + C::Q_OFF;  // stage s: Q at Q_OFF + s*2*TILE, dO right after
   uint8_t* sDS = smem + C::DS_OFF;
-  float* s_nlse2 = reinterpret_cast<float*>(smem + C::STAT_OFF);  // -lse2 per query of the step
-  float* s_ndrow = s_nlse2 + 128;                                  // -D per query of the step
+  // -lse2 and -D per query of a step (buffer it % NSTAT)
+  auto s_nlse2 = [&](int it) { return reinterpret_cast<float*>(smem + C::STAT_OFF) + (it % C::NSTAT) * 256; };
+  auto s_ndrow = [&](int it) { return s_nlse2(it) + 128; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;     // [2]
@@ -285,6 +302,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* dq_free = bars + 10;   // dQ_i read out
   uint64_t* acc_done = bars + 11;  // every MMA completed: dK, dV final
   uint64_t* stat_full = bars + 12; // the step's lse / D staged in shared memory
+  uint64_t* st_free = bars + 13;   // S^T and dP^T of a step loaded by every softmax-grad thread (EARLY_S)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -314,6 +332,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     mbar_init(dq_free, 128);
     mbar_init(acc_done, 1);
     mbar_init(stat_full, BWD_SG_THREADS);
+    mbar_init(st_free, BWD_SG_THREADS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -449,13 +468,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           mma_commit(q_empty + (it & 1));
         }
       };
-      if (!wait_bar(p_full, it & 1)) break;
+      if (!wait_bar(C::EARLY_S ? st_free : p_full, it & 1)) break;
       if constexpr (C::SEP) {
         // the softmax-grad has read S^T_i and dP^T_i: the next step's products may overwrite them
+        // (with EARLY_S as soon as every thread has loaded them, while the softmax-grad still runs)
         if (it + 1 < n_it) {
           if (!wait_bar(q_full + ((it + 1) & 1), ((it + 1) >> 1) & 1)) break;
           if (!issue_s_dp(it + 1)) break;
         }
+        if (C::EARLY_S && !wait_bar(p_full, it & 1)) break;
         issue_dv();
         // dQ_i into the dQ columns once the drain has read dQ_{i-1}
         if (it > 0 && !wait_bar(dq_free, (it - 1) & 1)) break;
@@ -500,7 +521,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // one entry of the per-row statistics (h = 0: lse2, h = 1: D) of query
     // row `row` of the Q tile, loaded one step ahead
     const float* stat_src = h ? p.drow : p.lse2;
-    float* stat_dst = (h ? s_ndrow : s_nlse2) + row;
+    auto stat_dst = [&](int it) { return (h ? s_ndrow(it) : s_nlse2(it)) + row; };
     float nx = 0.f;
     auto fetch = [&](int it) {
       const int qi = (qt0 + it) * 128 + row;
@@ -514,9 +535,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // stage this Q tile's statistics, negated; every thread of the previous
-      // step has finished with them (s_full needed all of p_full)
-      *stat_dst = -nx;
+      // stage this Q tile's statistics, negated; every thread has finished
+      // with the buffer's previous contents (s_full of this step needed all of
+      // p_full of the previous one, or with EARLY_S and two buffers st_free
+      // of the previous step, which every thread reaches after step it - 2)
+      *stat_dst(it) = -nx;
       fetch(it + 1);
       mbar_arrive(stat_full);  // release: this thread's value is visible to the waiters
       // the statistics are waited for once the first TMEM loads are in flight
@@ -551,11 +574,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // lse = +inf, so their weights are 0 without a test.
       if ((p.causal && k0 + 127 - delta > q0) || k0 + 128 > p.Nk) {
         const int c_lo = kabs >= p.Nk ? INT_MAX : (p.causal ? kabs - delta - q0 : INT_MIN);
-        ok = sg_half<D, true>(tST, tDPT, tPT, ds_row(it), row, h, c_lo, s_nlse2, s_ndrow, p.scale_log2, before_math,
-                              before_pstore, before_store);
+        ok = sg_half<D, true>(tST, tDPT, tPT, ds_row(it), row, h, c_lo, s_nlse2(it), s_ndrow(it), p.scale_log2,
+                              before_math, before_pstore, before_store, C::EARLY_S ? st_free : nullptr);
       } else {
-        ok = sg_half<D, false>(tST, tDPT, tPT, ds_row(it), row, h, 0, s_nlse2, s_ndrow, p.scale_log2, before_math,
-                               before_pstore, before_store);
+        ok = sg_half<D, false>(tST, tDPT, tPT, ds_row(it), row, h, 0, s_nlse2(it), s_ndrow(it), p.scale_log2,
+                               before_math, before_pstore, before_store, C::EARLY_S ? st_free : nullptr);
       }
       if (!ok) break;
       tmem_st_wait();
