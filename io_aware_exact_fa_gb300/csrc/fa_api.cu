@@ -23,7 +23,7 @@
 #include "fa_debug.cuh"
 
 // Causal unit order for K/V larger than L2 (see below): off by default. With a
-// 40 MB budget the long-context launches read 1.0x their Q+K+V from DRAM
+// 40 MB budget the long-context launches read 1.3x their Q+K+V from DRAM
 // instead of 2.7x (B=1 H=32 N=8192 d=128: 268 against 545 MB) but ran 6 %
 // slower (1,166 against 1,243 TFLOP/s; 32k: 1,293 against 1,364): the
 // pair-major order over all heads is faster, and DRAM runs at 17 % of its
@@ -279,7 +279,8 @@ fa_status prefill_common(const void* q, const void* k, const void* v, void* o, f
     for (float x : {f8.dq, f8.dk, f8.dv})
       if (!std::isfinite(x) || !(x > 0.f)) return fail(FA_ERR_INVALID_ARG, "descale factors must be finite and > 0");
     if (!std::isfinite(scale * f8.dq * f8.dk)) return fail(FA_ERR_INVALID_ARG, "scale * descale_q * descale_k overflows");
-    if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported for e4m3 inputs (64 or 128)", d);
+    if (d != 64 && d != 128)
+      return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported for e4m3 inputs (64 or 128)", d);
   }
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d unsupported (64 or 128)", d);
   if (Nq == 0) return FA_OK;  // nothing to compute (an empty q may have a NULL data pointer)
