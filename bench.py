@@ -467,6 +467,17 @@ def run_materialized(args, fa, wp, modes, q, k, v, flush, stream, warm, world, d
     return out
 
 
+def grouped_decode_kernel(w):
+    """The split kernel fa_decode_grouped launches for a workload: by the
+    number of query rows per K/V head, (H / Hkv) * Nq, and the head dim."""
+    rows = w.H // w.Hkv * w.Nq
+    if w.d == 64 and rows <= 4:
+        return f"fa_decode_grouped_cc_kernel<64, {1 if rows == 1 else 2 if rows == 2 else 4}>"
+    if w.d == 128 and rows <= 16:
+        return "fa_decode_grouped_kt_kernel"
+    return f"fa_decode_grouped_kernel<{w.d}>"
+
+
 def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
     """Time fa_decode_grouped on each decode-variant workload (grouped K/V
     heads, ragged lengths, 1 or 4 new tokens). Inputs are drawn on the device
@@ -521,7 +532,7 @@ def run_decode_variants(args, fa, W, stream, warm, world, rank, dev):
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": ach / peaks["hbm_gbs"],
                          "traffic": recorded_traffic("decode_grouped_sm103.cu", w.name),
-                         "kernel": f"fa_decode_grouped_kernel<{w.d}> + fa_decode_merge_kernel<{w.d}>",
+                         "kernel": f"{grouped_decode_kernel(w)} + fa_decode_merge_kernel<{w.d}>",
                          "peak_source": f"{peaks['source']} copy",
                          "bytes_convention": "visible K and V rows read once, q and o written, lse"},
         }

@@ -211,8 +211,9 @@ size_t fa_decode_grouped_workspace_size(int B, int H, int Nq, int d, int num_spl
  * Sequence b holds L_b = seqlens_k[b] keys (clamped to [0, Nk]; all Nk when
  * seqlens_k is NULL), and its Nq new tokens are its last Nq positions: token t
  * sees key j iff j < L_b and j <= L_b - Nq + t. A token that sees no key gets
- * o = 0 and lse = -inf. The (H/Hkv)*Nq query rows of one (b, K/V head) form
- * one tensor-core tile, so each K/V byte is read once per group.
+ * o = 0 and lse = -inf. The (H/Hkv)*Nq query rows of one (b, K/V head) read
+ * the K/V stream together, so each K/V byte is read once per group: up to four
+ * rows on the CUDA cores (packed fp32 products), more in one tensor-core tile.
  *   q, o       bf16 [B, H, Nq, d]      k_cache, v_cache  bf16 [B, Hkv, Nk, d]
  *   seqlens_k  int32 [B] in device memory, or NULL
  *   lse        fp32 [B, H, Nq] (may be NULL)

@@ -1,5 +1,6 @@
-// Parameters and launcher of the tensor-core split-KV decode for grouped K/V
-// heads, several query tokens per sequence and per-sequence KV lengths.
+// Parameters and launcher of the split-KV decode for grouped K/V heads, several
+// query tokens per sequence and per-sequence KV lengths (tensor-core kernels,
+// and a CUDA-core kernel for groups of at most four query rows).
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -10,6 +11,9 @@
 namespace fa {
 
 struct DecodeGroupedParams {
+  const void* q;             // bf16 [B, H, Nq, d]       (read by the CUDA-core kernel; the others use tensor maps)
+  const void* k;             // bf16 [B, Hkv, Nk, d]
+  const void* v;             // bf16 [B, Hkv, Nk, d]
   const int* seqlens;        // int32 [B] keys per sequence (device), or nullptr: every sequence has Nk
   float* ws_o;               // fp32 [B*H*Nq, S, d]  unnormalised partial outputs
   float* ws_ml;              // fp32 [B*H*Nq, S, 2]  partial (reference max in log2 units, sum)

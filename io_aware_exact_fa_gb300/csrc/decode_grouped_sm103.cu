@@ -45,13 +45,14 @@ constexpr int DG_SM_WARP0 = 4;  // warps 4-7
 // (log2 units), so the weights stay below 2^8 and O is rescaled rarely.
 constexpr float DG_RESCALE_THRESHOLD = 8.0f;
 
-// Wait used only to drain: returns when the phase completed or the limit ran out.
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+// Wait used only to drain: returns true when the phase completed, false when
+// the limit ran out first.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(a, parity)) return;
-    if ((i & 31u) == 31u && globaltimer_ns() - t0 > limit_ns) return;
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 31u) == 31u && globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -792,6 +793,342 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
   }
 }
 
+// ---------------------------------------------------------------------------
+// fa_decode_grouped_cc_kernel<D, RP>: the same split-KV decode for groups of
+// R <= RP <= 4 query rows per K/V head (one new token with up to four query
+// heads per K/V head). With so few rows each K/V element feeds R multiply-adds
+// per product, well below what the CUDA cores sustain at HBM speed, while a
+// 128-lane tensor-core tile would be mostly padding; so the products run on
+// the CUDA cores in packed fp32x2 and the kernel is a plain stream. The
+// launcher takes it at d = 64 (the 128-row tensor-core kernel streams at about
+// 0.6 of its rate there); at d = 128 the keys-on-lanes tensor-core kernel
+// measured faster than this one and is used instead.
+//   warp 4     producer: one lane moves KT keys of K and KT keys of V per stage
+//              into a ring of NST shared-memory stages with 1-D bulk copies
+//              (cp.async.bulk, completion counted on the stage's mbarrier).
+//   warps 0-3  consumers: warp w takes U rounds of KPW keys of each stage. A
+//              key row (D bf16) is read by LPK = D/8 lanes, 16 bytes each, so
+//              one warp-wide shared load covers 512 contiguous bytes. A lane
+//              forms the partial dots of its 8 columns with the RP query rows;
+//              a halving exchange over the key's lanes leaves each lane the
+//              full score of one row (its own row), which it turns into a
+//              weight against that row's reference max; the RP weights are
+//              then broadcast over the key's lanes and every lane accumulates
+//              its 8 columns of o for all rows.
+// Online state per lane group (the lanes of one key): per row a reference max
+// in log2 units, moved lazily as in the tensor-core kernels, a sum and an
+// o-slice. At the end the groups are combined through shared memory and the
+// split writes its unnormalised partial (o, m, l) like the other kernels.
+namespace {
+
+#ifndef FA_DGC_NW
+#define FA_DGC_NW 4    // consumer warps of the CUDA-core kernel
+#endif
+#ifndef FA_DGC_U
+#define FA_DGC_U 4     // key rounds per consumer warp and stage
+#endif
+#ifndef FA_DGC_NST
+#define FA_DGC_NST 3   // shared-memory stages
+#endif
+#ifndef FA_DGC_MINB
+#define FA_DGC_MINB 3  // CTAs per SM the registers and shared memory are sized for
+#endif
+constexpr int DGC_NW = FA_DGC_NW;
+constexpr int DGC_THREADS = 32 * (DGC_NW + 1);  // + the producer warp
+constexpr int DGC_U = FA_DGC_U;
+constexpr uint32_t DGC_FULL = 0xffffffffu;
+constexpr uint32_t DGC_BAR_ID = 1;  // named barrier of all the CTA's warps at the end
+
+template <int D, int RP>
+struct DgcCfg {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
+  static_assert(RP == 1 || RP == 2 || RP == 4, "1, 2 or 4 query rows");
+  static constexpr int LPK = D / 8;                  // lanes per key row
+  static constexpr int KPW = 32 / LPK;               // keys per warp-wide round
+  static constexpr int KT = DGC_NW * DGC_U * KPW;    // keys per stage
+  static constexpr int ROW = D * 2;                  // bytes of a key row
+  static constexpr int STAGE = 2 * KT * ROW;         // K rows, then V rows
+  static constexpr int NST = FA_DGC_NST;
+  static constexpr int NG = DGC_NW * KPW;            // lane groups of the CTA
+  // at the end the stages hold the groups' states: float [NG][RP][D] o-slices, then [NG][RP][2] (m, l)
+  static constexpr int ACC_OFF = 0;
+  static constexpr int ML_OFF = ACC_OFF + NG * RP * D * 4;
+  static_assert(ML_OFF + NG * RP * 2 * 4 <= NST * STAGE, "the final states fit in the stages");
+  static constexpr int BAR_OFF = NST * STAGE;        // full[NST], empty[NST]
+  static constexpr int MISC_OFF = BAR_OFF + 2 * NST * 8;
+  static constexpr int SMEM = MISC_OFF + 16 + 128;   // + slack to align the base to 128
+  static_assert(FA_DGC_MINB * (SMEM + 1024) <= 228 * 1024, "shared memory for the CTAs per SM");
+};
+
+// Lane (within its key's LPK lanes) that holds the full score of row r after
+// dgc_reduce_own.
+template <int RP, int LPK>
+__device__ __forceinline__ int dgc_owner(int r) {
+  if constexpr (RP == 4) return (r >> 1) * (LPK / 2) + (r & 1) * (LPK / 4);
+  else if constexpr (RP == 2) return r * (LPK / 2);
+  else return 0;
+}
+
+// Sum of v[r] over the LPK lanes of a key, returning on lane li the sum for
+// its own row (dgc_owner(own) has the same bits as li in the halving
+// positions). The first log2(RP) steps halve the values a lane carries (it
+// keeps one half and sends the other to its partner); the rest are plain
+// butterfly steps, so the LPK / RP lanes of a row end with the same sum.
+template <int RP, int LPK>
+__device__ __forceinline__ float dgc_reduce_own(const float (&v)[RP], int li) {
+  constexpr int REST = RP == 4 ? LPK / 8 : RP == 2 ? LPK / 4 : LPK / 2;  // plain steps after the halving
+  float x;
+  if constexpr (RP == 4) {
+    const bool ha = (li & (LPK / 2)) != 0;
+    const float w0 = (ha ? v[2] : v[0]) + __shfl_xor_sync(DGC_FULL, ha ? v[0] : v[2], LPK / 2);
+    const float w1 = (ha ? v[3] : v[1]) + __shfl_xor_sync(DGC_FULL, ha ? v[1] : v[3], LPK / 2);
+    const bool hb = (li & (LPK / 4)) != 0;
+    x = (hb ? w1 : w0) + __shfl_xor_sync(DGC_FULL, hb ? w0 : w1, LPK / 4);
+  } else if constexpr (RP == 2) {
+    const bool ha = (li & (LPK / 2)) != 0;
+    x = (ha ? v[1] : v[0]) + __shfl_xor_sync(DGC_FULL, ha ? v[0] : v[1], LPK / 2);
+  } else {
+    x = v[0];
+  }
+#pragma unroll
+  for (int off = REST; off >= 1; off >>= 1) x += __shfl_xor_sync(DGC_FULL, x, off);
+  return x;
+}
+
+template <int RP, int LPK>
+__device__ __forceinline__ int dgc_own_row(int li) {
+  if constexpr (RP == 4) return ((li & (LPK / 2)) ? 2 : 0) + ((li & (LPK / 4)) ? 1 : 0);
+  else if constexpr (RP == 2) return (li & (LPK / 2)) ? 1 : 0;
+  else return 0;
+}
+
+// Two consecutive bf16 (the low half first) as an fp32 pair.
+__device__ __forceinline__ uint64_t dgc_bf16x2_f2(uint32_t w) {
+  return f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint4 dgc_lds128(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+
+// exp2(m - M), 0 for a part that saw no key (m = -inf).
+__device__ __forceinline__ float dgc_rebase(float m, float M) { return m == -INFINITY ? 0.f : ex2_approx(m - M); }
+
+}  // namespace
+
+template <int D, int RP>
+__global__ void __launch_bounds__(DGC_THREADS, FA_DGC_MINB) fa_decode_grouped_cc_kernel(const DecodeGroupedParams p) {
+  using C = DgcCfg<D, RP>;
+  constexpr int LPK = C::LPK, KPW = C::KPW, KT = C::KT, NST = C::NST, ROW = C::ROW;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);  // [NST] stage landed
+  uint64_t* empty = full + NST;                                      // [NST] stage read by the 4 consumer warps
+  float* sacc = reinterpret_cast<float*>(smem + C::ACC_OFF);
+  float* sml = reinterpret_cast<float*>(smem + C::ML_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF);
+  volatile int* drained = abort_flag + 1;  // every copy the producer issued has landed
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t lim = p.wait_limit_ns;
+  const int s = static_cast<int>(blockIdx.x) % p.S;
+  const int bg = static_cast<int>(blockIdx.x) / p.S;  // b * Hkv + g
+  const int b = bg / p.Hkv;
+  const int g = bg % p.Hkv;
+  const int L = p.seqlens ? min(max(p.seqlens[b], 0), p.Nk) : p.Nk;
+  const int k0 = s * p.chunk;
+  const int k1 = min(L, k0 + p.chunk);
+  const int n = k1 > k0 ? (k1 - k0 + KT - 1) / KT : 0;  // stages of this split
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, DGC_NW);
+    }
+    *abort_flag = 0;
+    *drained = 1;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const size_t kv_off = static_cast<size_t>(bg) * p.Nk * ROW;  // bytes to this (b, K/V head)'s rows
+  const size_t row0 = (static_cast<size_t>(b) * p.H + static_cast<size_t>(g) * p.G) * p.Nq;  // first query row
+  const int sub = lane / LPK;  // key of the round within the warp
+  const int li = lane % LPK;   // 16-byte slice of the key row
+  const int gi = warp * KPW + sub;
+
+  if (warp == DGC_NW) {
+    // ---- producer: stage i holds keys [k0 + i KT, min(k1, k0 + (i + 1) KT))
+    if (lane == 0) {
+      const uint8_t* kg = static_cast<const uint8_t*>(p.k) + kv_off;
+      const uint8_t* vg = static_cast<const uint8_t*>(p.v) + kv_off;
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int st = i % NST;
+        if (i >= NST && !mbar_wait(empty + st, ((i / NST) - 1) & 1, lim, p.status, abort_flag)) break;
+        const int key = k0 + i * KT;
+        const uint32_t bytes = static_cast<uint32_t>(min(KT, k1 - key) * ROW);
+        uint8_t* dst = smem + st * C::STAGE;
+        mbar_arrive_expect_tx(full + st, 2 * bytes);
+        bulk_load_1d(dst, kg + static_cast<size_t>(key) * ROW, bytes, full + st);
+        bulk_load_1d(dst + KT * ROW, vg + static_cast<size_t>(key) * ROW, bytes, full + st);
+        issued = i + 1;
+      }
+      // no copy may still be writing shared memory when it is reused or the CTA exits
+      for (int i = max(0, issued - NST); i < issued; ++i)
+        if (!mbar_drain(full + i % NST, (i / NST) & 1, lim)) *drained = 0;
+    }
+    __syncwarp();
+    named_bar_sync(DGC_BAR_ID, DGC_THREADS);  // the stages are free
+  } else {
+    // ---- consumers
+    // query rows of this group, columns li*8 .. li*8+7, in log2 units with the scale's sign
+    const float qs = p.negate_s ? -p.scale_log2 : p.scale_log2;
+    uint64_t q2[RP][4];
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (r < p.R)
+        w = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (row0 + r) * D + li * 8);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q2[r][i] = fmul2(dgc_bf16x2_f2(ww[i]), f2pack(qs, qs));
+    }
+    // row r (head g G + r / Nq, token r % Nq) sees key j iff j < L - Nq + 1 + r % Nq
+    const int own = dgc_own_row<RP, LPK>(li);
+    const int lim_own = own < p.R ? min(k1, L - p.Nq + 1 + own % p.Nq) : k0;
+    const int base_lane = lane & ~(LPK - 1);
+    float m_own = -INFINITY, l_own = 0.f;
+    uint64_t acc[RP][4];
+#pragma unroll
+    for (int r = 0; r < RP; ++r)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[r][i] = 0ull;
+
+    for (int i = 0; i < n; ++i) {
+      const int st = i % NST;
+      if (!__all_sync(DGC_FULL, mbar_wait(full + st, (i / NST) & 1, lim, p.status, abort_flag))) break;
+      const int kl0 = warp * (DGC_U * KPW) + sub;  // stage-local key of round 0
+      const int key0 = k0 + i * KT + kl0;
+      const uint32_t ks = smem_u32(smem + st * C::STAGE) + kl0 * ROW + li * 16;
+      const uint32_t vs = ks + KT * ROW;
+      uint4 kr[DGC_U], vr[DGC_U];
+#pragma unroll
+      for (int u = 0; u < DGC_U; ++u) {
+        if (key0 + u * KPW < k1) {  // the rows past the split's end were not copied
+          kr[u] = dgc_lds128(ks + u * KPW * ROW);
+          vr[u] = dgc_lds128(vs + u * KPW * ROW);
+        } else {
+          kr[u] = make_uint4(0, 0, 0, 0);
+          vr[u] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      float x[DGC_U];
+#pragma unroll
+      for (int u = 0; u < DGC_U; ++u) {
+        const uint64_t k2[4] = {dgc_bf16x2_f2(kr[u].x), dgc_bf16x2_f2(kr[u].y), dgc_bf16x2_f2(kr[u].z),
+                                dgc_bf16x2_f2(kr[u].w)};
+        float dv[RP];
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+          uint64_t d2 = fmul2(q2[r][0], k2[0]);
+          d2 = ffma2(q2[r][1], k2[1], d2);
+          d2 = ffma2(q2[r][2], k2[2], d2);
+          d2 = ffma2(q2[r][3], k2[3], d2);
+          float lo, hi;
+          f2unpack(d2, lo, hi);
+          dv[r] = lo + hi;
+        }
+        const float sc = dgc_reduce_own<RP, LPK>(dv, li);
+        x[u] = (key0 + u * KPW < lim_own) ? sc : -INFINITY;
+      }
+      // lazy reference max of the own row
+      float mx = x[0];
+#pragma unroll
+      for (int u = 1; u < DGC_U; ++u) mx = fmaxf(mx, x[u]);
+      float alpha_own = 1.f;
+      bool moved = false;
+      if (mx > m_own + DG_RESCALE_THRESHOLD) {
+        if (m_own != -INFINITY) {
+          alpha_own = ex2_approx(m_own - mx);
+          moved = true;
+        }
+        m_own = mx;
+        l_own *= alpha_own;
+      }
+      if (__any_sync(DGC_FULL, moved)) {
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+          const float a = __shfl_sync(DGC_FULL, alpha_own, base_lane + dgc_owner<RP, LPK>(r));
+          const uint64_t a2 = f2pack(a, a);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[r][j] = fmul2(acc[r][j], a2);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < DGC_U; ++u) {
+        const float pu = (m_own == -INFINITY) ? 0.f : ex2_approx(x[u] - m_own);  // x = -inf -> 0
+        l_own += pu;
+        const uint64_t v2[4] = {dgc_bf16x2_f2(vr[u].x), dgc_bf16x2_f2(vr[u].y), dgc_bf16x2_f2(vr[u].z),
+                                dgc_bf16x2_f2(vr[u].w)};
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+          const float pr = __shfl_sync(DGC_FULL, pu, base_lane + dgc_owner<RP, LPK>(r));
+          const uint64_t p2 = f2pack(pr, pr);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[r][j] = ffma2(p2, v2[j], acc[r][j]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + st);
+    }
+    // this group's state to shared memory (over the stages, once every copy
+    // landed): o-slices from every lane, (m, l) of each row from that row's
+    // first owner lane
+    named_bar_sync(DGC_BAR_ID, DGC_THREADS);
+    if (*drained) {
+#pragma unroll
+      for (int r = 0; r < RP; ++r) {
+        float o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f2unpack(acc[r][j], o[2 * j], o[2 * j + 1]);
+        float4* dst = reinterpret_cast<float4*>(sacc + (gi * RP + r) * D + li * 8);
+        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+      }
+      if (li == dgc_owner<RP, LPK>(own)) {
+        sml[(gi * RP + own) * 2 + 0] = m_own;
+        sml[(gi * RP + own) * 2 + 1] = l_own;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- combine the NG groups: one thread per (row, column); after a timeout
+  // (*drained = 0) the stages may still change, so nothing is combined
+  for (int idx = threadIdx.x; *drained && idx < p.R * D; idx += DGC_THREADS) {
+    const int r = idx / D, c = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < C::NG; ++t) M = fmaxf(M, sml[(t * RP + r) * 2]);
+    float o = 0.f, l = 0.f;
+#pragma unroll
+    for (int t = 0; t < C::NG; ++t) {
+      const float f = dgc_rebase(sml[(t * RP + r) * 2], M);
+      o = fmaf(sacc[(t * RP + r) * D + c], f, o);
+      l = fmaf(sml[(t * RP + r) * 2 + 1], f, l);
+    }
+    const size_t part = (row0 + r) * p.S + s;
+    p.ws_o[part * D + c] = o;
+    if (c == 0) {
+      p.ws_ml[part * 2 + 0] = M;
+      p.ws_ml[part * 2 + 1] = l;
+    }
+  }
+}
+
 template <int D>
 static cudaError_t launch_decode_grouped_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                            const DecodeGroupedParams& p, cudaStream_t stream) {
@@ -818,15 +1155,51 @@ static cudaError_t launch_decode_grouped_t(const CUtensorMap& tq, const CUtensor
 using DgtKernel = DgtCfg<FA_DGT_NK, FA_DGT_NV, FA_DGT_NPB>;
 #define FA_DGT_KERNEL fa_decode_grouped_kt_kernel<FA_DGT_NK, FA_DGT_NV, FA_DGT_NPB, FA_DGT_MINB>
 
+#ifndef FA_DGC_ENABLE
+#define FA_DGC_ENABLE 1
+#endif
+// Groups of at most four query rows stream through the CUDA-core kernel at d = 64.
+static bool use_cc(int d, int R) { return FA_DGC_ENABLE && d == 64 && R <= 4; }
 // The keys-on-lanes kernel takes d = 128 with at most 16 query rows per K/V head.
 static bool use_kt(int d, int R) { return FA_DGT_ENABLE && d == 128 && R <= DGT_NP; }
+
+template <int D, int RP>
+static cudaError_t launch_cc(const DecodeGroupedParams& p, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.S);
+  fa_decode_grouped_cc_kernel<D, RP><<<grid, DGC_THREADS, DgcCfg<D, RP>::SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_cc_d(const DecodeGroupedParams& p, cudaStream_t stream) {
+  if (p.R == 1) return launch_cc<D, 1>(p, stream);
+  if (p.R == 2) return launch_cc<D, 2>(p, stream);
+  return launch_cc<D, 4>(p, stream);
+}
+
+template <int D, int RP>
+static cudaError_t set_cc_attributes() {
+  return cudaFuncSetAttribute(fa_decode_grouped_cc_kernel<D, RP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DgcCfg<D, RP>::SMEM);
+}
+
+template <int D>
+static cudaError_t set_cc_attributes_d() {
+  cudaError_t e = set_cc_attributes<D, 1>();
+  if (e == cudaSuccess) e = set_cc_attributes<D, 2>();
+  if (e == cudaSuccess) e = set_cc_attributes<D, 4>();
+  return e;
+}
 
 int decode_grouped_q_box_rows(int d, int R) { return use_kt(d, R) ? DGT_NP : 128; }
 
 cudaError_t decode_grouped_set_attributes(int d) {
-  if (d == 64)
+  if (d == 64) {
+    const cudaError_t e = set_cc_attributes_d<64>();
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(fa_decode_grouped_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 DgCfg<64>::SMEM);
+  }
   cudaError_t e = cudaFuncSetAttribute(fa_decode_grouped_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DgCfg<128>::SMEM);
   if (e != cudaSuccess) return e;
@@ -835,6 +1208,7 @@ cudaError_t decode_grouped_set_attributes(int d) {
 
 cudaError_t launch_decode_grouped(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const DecodeGroupedParams& p, cudaStream_t stream) {
+  if (use_cc(d, p.R)) return launch_cc_d<64>(p, stream);
   if (use_kt(d, p.R)) {
     const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.S);
     FA_DGT_KERNEL<<<grid, DGT_THREADS, DgtKernel::SMEM, stream>>>(tq, tk, tv, p);

@@ -345,15 +345,17 @@ fa_status prefill_common(const void* q, const void* k, const void* v, void* o, f
     // Causal order: when all heads' K/V exceed the L2 budget, walk bands of
     // pair lengths head by head, with bands wide enough that the units running
     // at once (one per SM) touch about budget / (K/V of a head) heads.
+    p.band = 0;
+#if FA_PREFILL_L2_BUDGET_MB > 0
     const double kv_head = 2.0 * Nk * d * (f8.on ? 1.0 : 2.0);
     const double budget = FA_PREFILL_L2_BUDGET_MB * 1048576.0;
-    p.band = 0;
-    if (causal && FA_PREFILL_L2_BUDGET_MB > 0 && kv_head * static_cast<double>(BH) > budget) {
+    if (causal && kv_head * static_cast<double>(BH) > budget) {
       const long long want = static_cast<long long>(std::ceil(static_cast<double>(G) * kv_head / budget));
       long long band = 1;
       while (band < want) band *= 2;
       p.band = static_cast<int>(std::min<long long>(band, n_qpairs));
     }
+#endif
   }
   cudaError_t e = fa::launch_prefill(d, f8.on, tq, tk, tv, to, p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
@@ -572,6 +574,9 @@ fa_status fa_decode_grouped(const void* q, const void* k_cache, const void* v_ca
   float* ws_o = static_cast<float*>(workspace);
   float* ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((parts * d * 4 + 255) & ~size_t(255)));
   fa::DecodeGroupedParams p{};
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
   p.seqlens = seqlens_k;
   p.ws_o = ws_o;
   p.ws_ml = ws_ml;

@@ -54,6 +54,10 @@ CASES = [
     (1, 32, 2, 8, 640, [640], 5),              # G = 16, 8 tokens: 128 rows per tile
     (2, 4, 2, 3, 130, [2, 130], 7),            # more splits than key tiles
     (2, 6, 3, 5, 257, [5, 256], 1),            # one split over several tiles, Nq = L for one sequence
+    (2, 4, 2, 1, 777, [777, 65], 3),           # G = 2: two rows per K/V head
+    (3, 6, 2, 1, 500, [0, 1, 500], 2),         # G = 3: three rows (a padded row), lengths 0 and 1
+    (2, 8, 4, 2, 900, [1, 899], 4),            # G = 2, 2 tokens: four rows; a length below Nq
+    (1, 2, 2, 3, 250, [250], 2),               # G = 1, 3 tokens
 ]
 
 
@@ -81,17 +85,18 @@ def test_decode_grouped_matches_splitkv_layout(fa):
     assert np.abs(l_g.reshape(-1) - to64(l_s).reshape(-1)).max() <= 2e-3
 
 
-def test_decode_grouped_offsets(fa):
+@pytest.mark.parametrize("Nq,d", [(2, 64), (1, 64), (1, 128)])
+def test_decode_grouped_offsets(fa, Nq, d):
     """Rows whose scores sit near +/-1e3 (through a constant last key component):
     the reference max handling must keep them finite and exact."""
-    B, H, Hkv, Nq, Nk, d = 1, 8, 2, 2, 700, 64
+    B, H, Hkv, Nk = 1, 8, 2, 700
     q, k, v = _inputs(B, H, Hkv, Nq, Nk, d, seed=77)
     scale = 1.0 / 8.0
     k = k.clone()
     k[..., -1] = 1.0
     qf = q.float()
     qf[0, 1, 0, -1] += 1e3 / scale
-    qf[0, 6, 1, -1] -= 1e3 / scale
+    qf[0, 6, Nq - 1, -1] -= 1e3 / scale
     q = qf.to(torch.bfloat16)
     lens = [650]
     o, lse = _run(fa, q, k, v, lens, 3, scale)
@@ -99,7 +104,7 @@ def test_decode_grouped_offsets(fa):
     compare(o.reshape(-1, d), lse.reshape(-1), o_ref.reshape(-1, d), lse_ref.reshape(-1), "offsets")
 
 
-@pytest.mark.parametrize("name", ["gqa", "gqa_spec"])
+@pytest.mark.parametrize("name", ["gqa", "gqa_spec", "gqa_d64"])
 def test_decode_grouped_full_size_sampled(fa, name):
     """The benchmark's workloads and inputs (seed 0): 48 seeded (b, h) heads, all tokens."""
     w = W.DECODE_VARIANTS[name]

@@ -2,9 +2,11 @@
 
 softmax(scale * Q K^T + mask) V is defined for any finite scale; with scale
 < 0 the largest weights go to the smallest dot products. The kernels that
-take a row maximum (prefill, grouped decode) run such a call as |scale|
-times scores that the score MMA negates; the split-KV decode scales q
-itself, and the backward pass takes no maximum. Every entry point is
+take a row maximum on the tensor cores (prefill, the tensor-core grouped
+decode kernels) run such a call as |scale| times scores that the score MMA
+negates; the split-KV decode and the CUDA-core grouped decode (d = 64, at
+most four query rows per K/V head) scale q itself, and the backward pass
+takes no maximum. Every entry point is
 checked here on ragged sizes, with the tolerances of the positive-scale
 tests.
 """
@@ -73,9 +75,10 @@ def test_split_decode_negative_scale(fa):
                   "split decode, negative scale"))
 
 
-def test_grouped_decode_negative_scale(fa):
+@pytest.mark.parametrize("Nq,d", [(3, 128), (1, 128), (1, 64)])
+def test_grouped_decode_negative_scale(fa, Nq, d):
     g = torch.Generator().manual_seed(23)
-    B, H, Hkv, Nq, Nk, d = 2, 8, 2, 3, 300, 128
+    B, H, Hkv, Nk = 2, 8, 2, 300
     q = torch.randn(B, H, Nq, d, generator=g).to(torch.bfloat16)
     k = torch.randn(B, Hkv, Nk, d, generator=g).to(torch.bfloat16)
     v = torch.randn(B, Hkv, Nk, d, generator=g).to(torch.bfloat16)
