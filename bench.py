@@ -473,8 +473,8 @@ def grouped_decode_kernel(w):
     rows = w.H // w.Hkv * w.Nq
     if w.d == 64 and rows <= 4:
         return f"fa_decode_grouped_cc_kernel<64, {1 if rows == 1 else 2 if rows == 2 else 4}>"
-    if w.d == 128 and rows <= 16:
-        return "fa_decode_grouped_kt_kernel"
+    if rows <= 16:
+        return f"fa_decode_grouped_kt_kernel<{w.d}>"
     return f"fa_decode_grouped_kernel<{w.d}>"
 
 

@@ -372,8 +372,12 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
 // the row max and sum over the 128 keys of a tile are warp reductions plus a
 // four-warp exchange.
 //
-// fa_decode_grouped_kt_kernel<NK, NV, NPB, MINB>: one CTA per (split, b, kv
-// head), 192 threads, registers sized for MINB CTAs per SM.
+// At d = 64 the value product keeps M = 128: a V stage holds two 64-column
+// boxes as at d = 128, the second zeroed once at the start and never loaded,
+// so O^T lanes 64-127 stay zero and only lanes 0-63 are written out.
+//
+// fa_decode_grouped_kt_kernel<D, NK, NV, NPB, MINB>: one CTA per (split, b,
+// kv head), 192 threads, registers sized for MINB CTAs per SM.
 //   warp 0     TMA producer: Q (16 rows) once, K tiles into a ring of NK
 //              stages, V tiles into a ring of NV stages.
 //   warp 1     TMEM allocator and MMA issuer (converged warp, elected lane):
@@ -384,23 +388,25 @@ __global__ void __launch_bounds__(DG_THREADS, 1)
 namespace {
 
 constexpr int DGT_NP = 16;        // query rows per tile (MMA N)
-constexpr int DGT_D = 128;
 constexpr uint32_t DGT_BAR_ID = 1;  // named barrier of the four softmax warps
 
 constexpr int DGT_THREADS = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr int DGT_SM_WARP0 = 2;
 
-template <int NK, int NV, int NPB>
+template <int D, int NK, int NV, int NPB>
 struct DgtCfg {
+  static_assert(D == 64 || D == 128, "head dim 64 or 128");
   static constexpr int NP = DGT_NP;
-  static constexpr int TILE = 128 * DGT_D * 2;  // one K or V tile: 128 keys x 128 bf16
-  static constexpr int BOX = 128 * 128;         // one TMA box of a K/V tile: 128 rows x 64 bf16
-  static constexpr int QBOX = NP * 128;         // one box of Q or P^T: NP rows x 64 bf16
-  static constexpr int Q_OFF = 0;               // Q: 2 boxes (d 0-63, 64-127)
-  static constexpr int P_OFF = Q_OFF + 2 * QBOX;  // P^T buffer b (of NPB): 2 boxes (keys 0-63, 64-127)
+  static constexpr int NBX = D / 64;             // 64-column boxes of a K/V row or a Q row
+  static constexpr int KV_BYTES = 128 * D * 2;   // one K or V tile: 128 keys x D bf16
+  static constexpr int V_STAGE = 128 * 128 * 2;  // a V stage: two boxes (the second zero at d = 64)
+  static constexpr int BOX = 128 * 128;          // one TMA box of a K/V tile: 128 rows x 64 bf16
+  static constexpr int QBOX = NP * 128;          // one box of Q or P^T: NP rows x 64 bf16
+  static constexpr int Q_OFF = 0;                // Q: NBX boxes
+  static constexpr int P_OFF = Q_OFF + NBX * QBOX;  // P^T buffer b (of NPB): 2 boxes (keys 0-63, 64-127)
   static constexpr int K_OFF = P_OFF + NPB * 2 * QBOX;
-  static constexpr int V_OFF = K_OFF + NK * TILE;
-  static constexpr int RED_OFF = V_OFF + NV * TILE;  // float [2][NP][4] row maxima per warp, [NP][4] row sums
+  static constexpr int V_OFF = K_OFF + NK * KV_BYTES;
+  static constexpr int RED_OFF = V_OFF + NV * V_STAGE;  // float [2][NP][4] row maxima per warp, [NP][4] row sums
   static constexpr int BAR_OFF = RED_OFF + 3 * NP * 4 * 4;
   static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 + 2 + 2 + NPB + 1 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
@@ -466,11 +472,11 @@ __device__ __forceinline__ void warp_reduce16(float* v, int lane) {
 
 }  // namespace
 
-template <int NK, int NV, int NPB, int MINB>
+template <int D, int NK, int NV, int NPB, int MINB>
 __global__ void __launch_bounds__(DGT_THREADS, MINB)
     fa_decode_grouped_kt_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                                 const __grid_constant__ CUtensorMap tmV, const DecodeGroupedParams p) {
-  using C = DgtCfg<NK, NV, NPB>;
+  using C = DgtCfg<D, NK, NV, NPB>;
   constexpr int NP = C::NP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -526,6 +532,14 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
+  if constexpr (D == 64) {
+    // the second box of every V stage: zeros, read by the value product
+    for (int i = threadIdx.x; i < NV * C::BOX / 16; i += DGT_THREADS) {
+      const int st = i / (C::BOX / 16), w = i % (C::BOX / 16);
+      st_shared_v4(smem_u32(smem + C::V_OFF + st * C::V_STAGE + C::BOX) + w * 16, 0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();  // the tensor core reads it through the async proxy
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -542,8 +556,8 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, 2 * C::QBOX);
-      for (int bx = 0; bx < 2; ++bx) tma_load_3d(smem + C::Q_OFF + bx * C::QBOX, &tmQ, q_full, 64 * bx, 0, bg);
+      mbar_arrive_expect_tx(q_full, C::NBX * C::QBOX);
+      for (int bx = 0; bx < C::NBX; ++bx) tma_load_3d(smem + C::Q_OFF + bx * C::QBOX, &tmQ, q_full, 64 * bx, 0, bg);
     }
     for (int j = 0; ok && j < n; ++j) {
       const int kt0 = k0 + j * 128;
@@ -552,9 +566,9 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
         if (!ok) break;
       }
       if (leader) {
-        uint8_t* dst = smem + C::K_OFF + (j % NK) * C::TILE;
-        mbar_arrive_expect_tx(k_full + j % NK, C::TILE);
-        for (int bx = 0; bx < 2; ++bx) tma_load_3d(dst + bx * C::BOX, &tmK, k_full + j % NK, 64 * bx, kt0, bg);
+        uint8_t* dst = smem + C::K_OFF + (j % NK) * C::KV_BYTES;
+        mbar_arrive_expect_tx(k_full + j % NK, C::KV_BYTES);
+        for (int bx = 0; bx < C::NBX; ++bx) tma_load_3d(dst + bx * C::BOX, &tmK, k_full + j % NK, 64 * bx, kt0, bg);
       }
       ++nk;
       if (j >= NV) {
@@ -562,9 +576,9 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
         if (!ok) break;
       }
       if (leader) {
-        uint8_t* dst = smem + C::V_OFF + (j % NV) * C::TILE;
-        mbar_arrive_expect_tx(v_full + j % NV, C::TILE);
-        for (int bx = 0; bx < 2; ++bx) tma_load_3d(dst + bx * C::BOX, &tmV, v_full + j % NV, 64 * bx, kt0, bg);
+        uint8_t* dst = smem + C::V_OFF + (j % NV) * C::V_STAGE;
+        mbar_arrive_expect_tx(v_full + j % NV, C::KV_BYTES);
+        for (int bx = 0; bx < C::NBX; ++bx) tma_load_3d(dst + bx * C::BOX, &tmV, v_full + j % NV, 64 * bx, kt0, bg);
       }
       ++nv;
     }
@@ -592,10 +606,10 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
     // MN-major K-step kk (16 keys of V): 16 rows = 2048 bytes in (the two 64-column boxes BOX apart)
     auto kmaj = [](int kk, int box) { return static_cast<uint32_t>(((kk >> 2) * box + (kk & 3) * 32) >> 4); };
     auto issue_s = [&](int j) {  // S^T_j = K_j Q^T into buffer j & 1
-      const uint32_t k_lo = sdesc_sw128_lo(smem_u32(smem + C::K_OFF + (j % NK) * C::TILE), 16);
+      const uint32_t k_lo = sdesc_sw128_lo(smem_u32(smem + C::K_OFF + (j % NK) * C::KV_BYTES), 16);
       const uint32_t tS = tmem + C::S_COL + (j & 1) * NP;
 #pragma unroll
-      for (int kk = 0; kk < DGT_D / 16; ++kk)
+      for (int kk = 0; kk < D / 16; ++kk)
         if (elect_one())
           mma_ss_w(tS, k_lo + kmaj(kk, C::BOX), DHI, q_lo + kmaj(kk, C::QBOX), DHI, idesc_s, kk > 0 ? 1u : 0u);
       if (elect_one()) {
@@ -604,7 +618,7 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
       }
     };
     auto issue_pv = [&](int j) {  // O^T += V_j^T P^T_j
-      const uint32_t v_lo = sdesc_sw128_lo(smem_u32(smem + C::V_OFF + (j % NV) * C::TILE), C::BOX);
+      const uint32_t v_lo = sdesc_sw128_lo(smem_u32(smem + C::V_OFF + (j % NV) * C::V_STAGE), C::BOX);
       const uint32_t p_lo = sdesc_sw128_lo(smem_u32(smem + C::P_OFF + (j % NPB) * 2 * C::QBOX), 16);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
@@ -770,10 +784,10 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
 #pragma unroll
       for (int r = 0; r < NP; ++r) {
         if (r == kr) m_mine = m_ref[r];
-        if (r < p.R) {
+        if (r < p.R && kr < D) {
           // query row (b, g * G + r / Nq, r % Nq) of [B, H, Nq]
           const size_t qrow = (static_cast<size_t>(b) * p.H + g * p.G + r / p.Nq) * p.Nq + r % p.Nq;
-          p.ws_o[(qrow * p.S + s) * DGT_D + kr] = __uint_as_float(ov[r]);
+          p.ws_o[(qrow * p.S + s) * D + kr] = __uint_as_float(ov[r]);
         }
       }
       if (kr < p.R) {
@@ -1152,16 +1166,26 @@ static cudaError_t launch_decode_grouped_t(const CUtensorMap& tq, const CUtensor
 #ifndef FA_DGT_ENABLE
 #define FA_DGT_ENABLE 1
 #endif
-using DgtKernel = DgtCfg<FA_DGT_NK, FA_DGT_NV, FA_DGT_NPB>;
-#define FA_DGT_KERNEL fa_decode_grouped_kt_kernel<FA_DGT_NK, FA_DGT_NV, FA_DGT_NPB, FA_DGT_MINB>
+template <int D>
+using DgtKernel = DgtCfg<D, FA_DGT_NK, FA_DGT_NV, FA_DGT_NPB>;
+#define FA_DGT_KERNEL(D) fa_decode_grouped_kt_kernel<D, FA_DGT_NK, FA_DGT_NV, FA_DGT_NPB, FA_DGT_MINB>
 
 #ifndef FA_DGC_ENABLE
 #define FA_DGC_ENABLE 1
 #endif
 // Groups of at most four query rows stream through the CUDA-core kernel at d = 64.
 static bool use_cc(int d, int R) { return FA_DGC_ENABLE && d == 64 && R <= 4; }
-// The keys-on-lanes kernel takes d = 128 with at most 16 query rows per K/V head.
-static bool use_kt(int d, int R) { return FA_DGT_ENABLE && d == 128 && R <= DGT_NP; }
+// The keys-on-lanes kernel takes the other groups of at most 16 query rows per K/V head
+// (at d = 64 with 5-16 rows it measured 4.46 TB/s against 3.53 for the 128-row kernel).
+static bool use_kt(int, int R) { return FA_DGT_ENABLE && R <= DGT_NP; }
+
+template <int D>
+static cudaError_t launch_kt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const DecodeGroupedParams& p, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.S);
+  FA_DGT_KERNEL(D)<<<grid, DGT_THREADS, DgtKernel<D>::SMEM, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
 
 template <int D, int RP>
 static cudaError_t launch_cc(const DecodeGroupedParams& p, cudaStream_t stream) {
@@ -1195,7 +1219,9 @@ int decode_grouped_q_box_rows(int d, int R) { return use_kt(d, R) ? DGT_NP : 128
 
 cudaError_t decode_grouped_set_attributes(int d) {
   if (d == 64) {
-    const cudaError_t e = set_cc_attributes_d<64>();
+    cudaError_t e = set_cc_attributes_d<64>();
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(FA_DGT_KERNEL(64), cudaFuncAttributeMaxDynamicSharedMemorySize, DgtKernel<64>::SMEM);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(fa_decode_grouped_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 DgCfg<64>::SMEM);
@@ -1203,17 +1229,13 @@ cudaError_t decode_grouped_set_attributes(int d) {
   cudaError_t e = cudaFuncSetAttribute(fa_decode_grouped_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DgCfg<128>::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(FA_DGT_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, DgtKernel::SMEM);
+  return cudaFuncSetAttribute(FA_DGT_KERNEL(128), cudaFuncAttributeMaxDynamicSharedMemorySize, DgtKernel<128>::SMEM);
 }
 
 cudaError_t launch_decode_grouped(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const DecodeGroupedParams& p, cudaStream_t stream) {
   if (use_cc(d, p.R)) return launch_cc_d<64>(p, stream);
-  if (use_kt(d, p.R)) {
-    const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.S);
-    FA_DGT_KERNEL<<<grid, DGT_THREADS, DgtKernel::SMEM, stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
-  }
+  if (use_kt(d, p.R)) return d == 64 ? launch_kt<64>(tq, tk, tv, p, stream) : launch_kt<128>(tq, tk, tv, p, stream);
   return d == 64 ? launch_decode_grouped_t<64>(tq, tk, tv, p, stream)
                  : launch_decode_grouped_t<128>(tq, tk, tv, p, stream);
 }

@@ -97,9 +97,11 @@ DECODE_VARIANTS = {
     # the same with 4 new (speculative) tokens per sequence
     "gqa_spec": DecodeVariant("decode_gqa_b64h32kv8nq4_nk8192d128_ragged", 64, 32, 8, 4, 8192, 128,
                               1.0 / math.sqrt(128.0), 4, 4096),
-    # one new token at head dim 64 (the prefill workload's head dim)
+    # one and four new tokens at head dim 64 (the prefill workload's head dim)
     "gqa_d64": DecodeVariant("decode_gqa_b64h32kv8nq1_nk8192d64_ragged", 64, 32, 8, 1, 8192, 64,
                              1.0 / 8.0, 4, 4096),
+    "gqa_spec_d64": DecodeVariant("decode_gqa_b64h32kv8nq4_nk8192d64_ragged", 64, 32, 8, 4, 8192, 64,
+                                  1.0 / 8.0, 4, 4096),
 }
 
 

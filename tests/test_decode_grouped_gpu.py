@@ -104,7 +104,7 @@ def test_decode_grouped_offsets(fa, Nq, d):
     compare(o.reshape(-1, d), lse.reshape(-1), o_ref.reshape(-1, d), lse_ref.reshape(-1), "offsets")
 
 
-@pytest.mark.parametrize("name", ["gqa", "gqa_spec", "gqa_d64"])
+@pytest.mark.parametrize("name", ["gqa", "gqa_spec", "gqa_d64", "gqa_spec_d64"])
 def test_decode_grouped_full_size_sampled(fa, name):
     """The benchmark's workloads and inputs (seed 0): 48 seeded (b, h) heads, all tokens."""
     w = W.DECODE_VARIANTS[name]
