@@ -74,6 +74,21 @@ def test_decode_grouped(fa, case, d):
     print(case, d, st)
 
 
+@pytest.mark.parametrize("d,Nq", [(64, 1), (64, 4), (128, 1)])
+def test_decode_grouped_deterministic(fa, d, Nq):
+    """Each split kernel (the CUDA-core kernel at d = 64 with one token, the
+    keys-on-lanes kernel otherwise) and the merge sum in a fixed order: two
+    calls on the same inputs give identical bytes."""
+    q, k, v = _inputs(2, 8, 2, Nq, 1500, d, seed=11)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    lens = torch.tensor([1500, 777], dtype=torch.int32, device="cuda")
+    o1, l1 = fa.decode_grouped(q, k, v, seqlens_k=lens, num_splits=3)
+    o2, l2 = fa.decode_grouped(q, k, v, seqlens_k=lens, num_splits=3)
+    torch.cuda.synchronize()
+    assert fa.device_status() == fa.FA_OK
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_decode_grouped_matches_splitkv_layout(fa):
     """G = 1, Nq = 1, no lengths: the same attention as fa_decode_splitkv (both
     against the oracle, and against each other within twice the tolerance)."""
