@@ -58,6 +58,8 @@ CASES = [
     (3, 6, 2, 1, 500, [0, 1, 500], 2),         # G = 3: three rows (a padded row), lengths 0 and 1
     (2, 8, 4, 2, 900, [1, 899], 4),            # G = 2, 2 tokens: four rows; a length below Nq
     (1, 2, 2, 3, 250, [250], 2),               # G = 1, 3 tokens
+    (2, 5, 1, 1, 400, [400, 130], 2),          # G = 5: one row past the CUDA-core kernel's four
+    (1, 17, 1, 1, 300, [300], 2),              # G = 17: one row past the keys-on-lanes kernel's sixteen
 ]
 
 
