@@ -842,7 +842,7 @@ namespace {
 #define FA_DGC_U 4     // key rounds per consumer warp and stage
 #endif
 #ifndef FA_DGC_NST
-#define FA_DGC_NST 3   // shared-memory stages
+#define FA_DGC_NST 4   // shared-memory stages
 #endif
 #ifndef FA_DGC_MINB
 #define FA_DGC_MINB 3  // CTAs per SM the registers and shared memory are sized for
