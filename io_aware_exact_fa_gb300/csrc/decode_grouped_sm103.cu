@@ -814,9 +814,9 @@ __global__ void __launch_bounds__(DGT_THREADS, MINB)
 // per product, well below what the CUDA cores sustain at HBM speed, while a
 // 128-lane tensor-core tile would be mostly padding; so the products run on
 // the CUDA cores in packed fp32x2 and the kernel is a plain stream. The
-// launcher takes it at d = 64 (the 128-row tensor-core kernel streams at about
-// 0.6 of its rate there); at d = 128 the keys-on-lanes tensor-core kernel
-// measured faster than this one and is used instead.
+// launcher takes it at d = 64 (there the keys-on-lanes tensor-core kernel
+// streams at about 0.8 of its rate, the 128-row one at 0.6); at d = 128 the
+// keys-on-lanes kernel measured faster than this one and is used instead.
 //   warp 4     producer: one lane moves KT keys of K and KT keys of V per stage
 //              into a ring of NST shared-memory stages with 1-D bulk copies
 //              (cp.async.bulk, completion counted on the stage's mbarrier).
